@@ -1,0 +1,278 @@
+"""Float64 CPU oracle for Palu-style G-LRD decode attention over cached latents.
+
+TEST INFRASTRUCTURE ONLY. This module exists to check the CUDA path. Only the
+test suite, the smoke check in ``__graft_entry__`` and the benchmark's CPU
+baseline / reference arm may import it. The library never imports it and has
+no CPU fallback.
+
+It is deliberately plain: NumPy float64, one (batch, head) at a time, every step
+in the order the pages state it, no blocking, fusion or reordering. Library
+primitives used as steps: ``numpy`` matmul, ``exp``/``log``, ``rint``, and the
+LAPACK SVD.
+
+Sources (page title, section):
+  [Palu]    "Palu: KV-Cache Compression With Low-Rank Projection" (paper notes)
+  [Puzzle]  "PuzzleKV: 基于页面的低秩分解用于KV缓存压缩" (translation)
+  [Shard]   "Shard - 实现10倍KV缓存压缩" (blog translation)
+
+Readings taken where the pages are silent (each is listed with its reason in the
+design notes):
+  * row-vector convention h = x A (the method section writes both h = Ax and
+    h = xA; A in R^{d x r} fixes h = xA);
+  * head i belongs to group i // s and is column block i % s of B_g;
+  * score scale 1/sqrt(d_h) on both paths;
+  * RoPE: rotate-half pairing (k, k + d_h/2) as [Shard] section 5 states for
+    Llama, inverse frequencies theta^(-2k/d_h) (the RoFormer schedule; the
+    [Palu] notes only cite RoFormer);
+  * the query arrives unrotated and is rotated at q_pos, which defaults to the
+    position of the last cached token; no mask (all cached tokens attend);
+  * the output stays in latent space, o_i = p_i H_v (B_v is fused into W_o);
+  * int4: per-token, per-group symmetric codes in [-7, 7], scale
+    fp16_rn(min(amax/7, 65504)) with amax and the division in IEEE fp32, codes
+    rint-half-even(h / scale) clamped to [-7, 7], zero codes when the scale is 0;
+    element 2j in the low nibble, 2j+1 in the high nibble (two's complement);
+  * an empty sequence yields o = 0 and lse = -inf.
+
+Every function below is pinned by a CPU test against something other than
+itself (closed forms, the pages' worked numbers, library routines, brute force,
+the identities the pages derive); none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+
+# ---------------------------------------------------------------------------
+# RoPE
+# ---------------------------------------------------------------------------
+
+def rope_inv_freq(head_dim: int, theta: float) -> np.ndarray:
+    """omega_k = theta^(-2k/d_h), k = 0 .. d_h/2-1 (RoFormer schedule cited by
+    [Palu] "方法细节", RoPE paragraph)."""
+    k = np.arange(head_dim // 2, dtype=np.float64)
+    return np.power(float(theta), -2.0 * k / head_dim)
+
+
+def rope_rotate(x: np.ndarray, pos, theta: float) -> np.ndarray:
+    """Rotate-half RoPE of the last axis of ``x`` at positions ``pos``.
+
+    [Shard] section 5, step 1 states Llama's inverse as
+    k_no_rope = k*cos(theta p) - rotate_half(k)*sin(theta p) with
+    rotate_half([a, b]) = [-b, a]; the forward map is therefore
+    out = x*cos + rotate_half(x)*sin, i.e. for each pair (a, b) = (x_k, x_{k+d/2}):
+    out_k = a cos - b sin, out_{k+d/2} = b cos + a sin.
+    ``pos`` broadcasts against x's leading axes.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    d = x.shape[-1]
+    half = d // 2
+    ang = np.asarray(pos, dtype=np.float64)[..., None] * rope_inv_freq(d, theta)
+    c, s = np.cos(ang), np.sin(ang)
+    a, b = x[..., :half], x[..., half:]
+    return np.concatenate([a * c - b * s, b * c + a * s], axis=-1)
+
+
+# ---------------------------------------------------------------------------
+# Softmax attention for one query head
+# ---------------------------------------------------------------------------
+
+def softmax_attend(scores: np.ndarray, values: np.ndarray):
+    """p = softmax(scores); returns (p @ values, lse) with lse = log sum exp(scores).
+
+    [Palu] "背景知识": p = Softmax(q K^T / sqrt(d_h)), a = p V. The max is
+    subtracted before exponentiating, which leaves p unchanged.
+    """
+    scores = np.asarray(scores, dtype=np.float64)
+    if scores.size == 0:
+        return np.zeros(values.shape[-1]), -math.inf
+    m = scores.max()
+    e = np.exp(scores - m)
+    l = e.sum()
+    p = e / l
+    return p @ values, m + math.log(l)
+
+
+# ---------------------------------------------------------------------------
+# Decode attention over G-LRD latents
+# ---------------------------------------------------------------------------
+
+def _group_of(head: int, group_size: int):
+    return head // group_size, head % group_size
+
+
+def _positions(positions, b: int, T: int):
+    if positions is None:
+        return np.arange(T, dtype=np.float64)
+    return np.asarray(positions[b][:T], dtype=np.float64)
+
+
+def _query_position(positions, q_pos, b: int, T: int):
+    if q_pos is not None:
+        return float(q_pos[b])
+    if positions is None:
+        return float(T - 1)
+    return float(positions[b][T - 1])
+
+
+def decode_rope_head(q_i, hk_bg, hv_bg, bk_g, j: int, pos, qp: float, theta: float):
+    """One head of the RoPE path.
+
+    Rebuild K_i = H_k,g B_g[:, j-block] ([Palu] "方法细节", G-LRD: the s heads of a
+    group are the column blocks of h_g B_g), rotate every key at its own position
+    and the query at qp, score q_rot K_rot^T / sqrt(d_h), softmax, and apply p to
+    the value latents (V rebuild skipped because B_v is fused into W_o, [Palu]
+    "方法细节", value fusion paragraph).
+    """
+    d_h = q_i.shape[-1]
+    T = hk_bg.shape[0]
+    if T == 0:
+        return np.zeros(hv_bg.shape[-1]), -math.inf
+    K = np.asarray(hk_bg, np.float64) @ np.asarray(bk_g, np.float64)[:, j * d_h:(j + 1) * d_h]
+    K_rot = rope_rotate(K, pos, theta)
+    q_rot = rope_rotate(np.asarray(q_i, np.float64), qp, theta)
+    scores = (K_rot @ q_rot) / math.sqrt(d_h)
+    return softmax_attend(scores, np.asarray(hv_bg, np.float64))
+
+
+def decode_absorbed_head(q_i, hk_bg, hv_bg, bk_g, j: int):
+    """One head of the non-RoPE path: the query is absorbed into the latent space,
+    q'_i = q_i (B_i^k)^T, and scored straight against H_k
+    ([Palu] "方法细节", key fusion: q_i K_i^T = q_i (H_i^k B_i^k)^T = (q_i B_i^k^T) H_i^k^T)."""
+    d_h = q_i.shape[-1]
+    if hk_bg.shape[0] == 0:
+        return np.zeros(hv_bg.shape[-1]), -math.inf
+    q_lat = np.asarray(bk_g, np.float64)[:, j * d_h:(j + 1) * d_h] @ np.asarray(q_i, np.float64)
+    scores = (np.asarray(hk_bg, np.float64) @ q_lat) / math.sqrt(d_h)
+    return softmax_attend(scores, np.asarray(hv_bg, np.float64))
+
+
+def decode(q, hk, hv, bk, seq_lens, group_size: int, *, mode: str = "rope", theta: float = 10000.0,
+           positions=None, q_pos=None, heads=None):
+    """Decode attention for every (batch, head), or only for ``heads`` = [(b, i), ...].
+
+    q  [B][n][d_h], hk [B][T][n_g][r_k], hv [B][T][n_g][r_v] (already dequantised),
+    bk [n_g][r_k][s*d_h], seq_lens [B]. Returns (o [B][n][r_v], lse [B][n]) float64;
+    entries not requested through ``heads`` are NaN.
+    """
+    B, n, _ = q.shape
+    r_v = hv.shape[-1]
+    o = np.full((B, n, r_v), np.nan)
+    lse = np.full((B, n), np.nan)
+    todo = heads if heads is not None else [(b, i) for b in range(B) for i in range(n)]
+    for b, i in todo:
+        T = int(seq_lens[b])
+        g, j = _group_of(i, group_size)
+        hk_bg = np.asarray(hk[b, :T, g, :], np.float64)
+        hv_bg = np.asarray(hv[b, :T, g, :], np.float64)
+        if mode == "rope":
+            pos = _positions(positions, b, T)
+            qp = _query_position(positions, q_pos, b, T) if T > 0 else 0.0
+            o[b, i], lse[b, i] = decode_rope_head(q[b, i], hk_bg, hv_bg, bk[g], j, pos, qp, theta)
+        elif mode == "absorbed":
+            o[b, i], lse[b, i] = decode_absorbed_head(q[b, i], hk_bg, hv_bg, bk[g], j)
+        else:
+            raise ValueError(mode)
+    return o, lse
+
+
+# ---------------------------------------------------------------------------
+# Uncompressed multi-head attention (the definition the latent path must equal)
+# ---------------------------------------------------------------------------
+
+def mha_decode(q, x, wk, wv, seq_lens, *, theta: float = 10000.0, rope: bool = True,
+               positions=None, q_pos=None):
+    """Plain MHA decode over cached activations x [B][T][d] ([Palu] "背景知识"):
+    k_i = x W_i^k, v_i = x W_i^v, p = softmax(q_i K_i^T / sqrt(d_h)), a_i = p V_i.
+    Returns a [B][n][d_h] and lse [B][n]."""
+    B, n, d_h = q.shape
+    a = np.zeros((B, n, d_h))
+    lse = np.zeros((B, n))
+    for b in range(B):
+        T = int(seq_lens[b])
+        xb = np.asarray(x[b, :T], np.float64)
+        pos = _positions(positions, b, T)
+        qp = _query_position(positions, q_pos, b, T)
+        for i in range(n):
+            K = xb @ wk[:, i * d_h:(i + 1) * d_h]
+            V = xb @ wv[:, i * d_h:(i + 1) * d_h]
+            qi = np.asarray(q[b, i], np.float64)
+            if rope:
+                K = rope_rotate(K, pos, theta)
+                qi = rope_rotate(qi, qp, theta)
+            a[b, i], lse[b, i] = softmax_attend(K @ qi / math.sqrt(d_h), V)
+    return a, lse
+
+
+# ---------------------------------------------------------------------------
+# Offline transforms the pins use
+# ---------------------------------------------------------------------------
+
+def svd_factor(w: np.ndarray, r: int):
+    """W ~= A B with A = U_r sqrt(S_r), B = sqrt(S_r) V_r^T ([Palu] "背景知识", SVD)."""
+    u, s, vt = np.linalg.svd(np.asarray(w, np.float64), full_matrices=False)
+    rs = np.sqrt(s[:r])
+    return u[:, :r] * rs[None, :], rs[:, None] * vt[:r]
+
+
+def hadamard(r: int) -> np.ndarray:
+    """Normalised Walsh-Hadamard matrix by Sylvester doubling, H_2m = [[H, H], [H, -H]],
+    scaled by 1/sqrt(r) so that R R^T = I ([Palu] "方法细节", Hadamard fold)."""
+    if r < 1 or r & (r - 1):
+        raise ValueError("r must be a power of two")
+    h = np.ones((1, 1))
+    while h.shape[0] < r:
+        h = np.block([[h, h], [h, -h]])
+    return h / math.sqrt(r)
+
+
+# ---------------------------------------------------------------------------
+# int4 per-token latent quantisation
+# ---------------------------------------------------------------------------
+
+FP16_MAX = 65504.0
+
+
+def quantize_int4(h):
+    """Per-token, per-group symmetric int4 codes ([Palu] "补充细节": simple per-token
+    quantisation of the latents; code range [-7, 7] as in [Shard] section 5, step 4).
+
+    h: float32 array [..., r]. Returns (codes int8 [..., r], scale float16 [...]).
+    Arithmetic in IEEE float32 / float16 round-to-nearest-even.
+    """
+    h = np.asarray(h, dtype=np.float32)
+    amax = np.max(np.abs(h), axis=-1)
+    q = np.minimum(amax / np.float32(7.0), np.float32(FP16_MAX)).astype(np.float32)
+    scale = q.astype(np.float16)
+    sf = scale.astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ratio = h / sf[..., None]
+    codes = np.clip(np.rint(ratio), -7, 7)
+    codes = np.where((sf == 0)[..., None], 0.0, codes).astype(np.int8)
+    return codes, scale
+
+
+def pack_int4(codes) -> np.ndarray:
+    """Two codes per byte: element 2j in bits 0-3, element 2j+1 in bits 4-7, each as
+    a 4-bit two's-complement number."""
+    c = np.asarray(codes, dtype=np.int16) & 0xF
+    return (c[..., 0::2] | (c[..., 1::2] << 4)).astype(np.uint8)
+
+
+def unpack_int4(packed) -> np.ndarray:
+    p = np.asarray(packed, dtype=np.uint8).astype(np.int16)
+    lo = p & 0xF
+    hi = (p >> 4) & 0xF
+    lo = np.where(lo >= 8, lo - 16, lo)
+    hi = np.where(hi >= 8, hi - 16, hi)
+    out = np.empty(p.shape[:-1] + (2 * p.shape[-1],), dtype=np.int8)
+    out[..., 0::2] = lo
+    out[..., 1::2] = hi
+    return out
+
+
+def dequant_int4(packed, scale) -> np.ndarray:
+    """Latent value = code * scale, returned in float64 (exact)."""
+    codes = unpack_int4(packed).astype(np.float64)
+    return codes * np.asarray(scale, dtype=np.float16).astype(np.float64)[..., None]

@@ -1,0 +1,216 @@
+"""Seeded synthetic workloads for Palu-style G-LRD decode attention.
+
+Every array here is a *draw*: random weights with a prescribed singular-value
+decay, their per-group truncated SVD factors (the offline weight transform that
+precedes decoding), Gaussian activations and queries. Nothing in this module
+computes attention, RoPE, softmax or quantisation; the oracle and the CUDA path
+both start from what it returns.
+
+Workload recipe (all five shapes follow the Llama-2-7B attention layer that the
+Palu notes evaluate, "实验环境"/"实验结果"):
+  * W_k, W_v = U diag(sigma) V^T with Haar-orthogonal U, V (QR of a Gaussian
+    matrix with the sign of R's diagonal folded into Q) and sigma_i = exp(-i/tau).
+  * Group g holds consecutive heads g*s .. g*s+s-1, W_g = W[:, g*s*d_h:(g+1)*s*d_h]
+    (the d x (d_h*s) concatenation of the G-LRD section of the Palu notes; 4096x512
+    for Llama-2-7B with s=4).
+  * Truncated SVD per group: A_g = U_r sqrt(S_r), B_g = sqrt(S_r) V_r^T
+    (Palu notes, "背景知识", SVD paragraph).
+  * Optional normalised Walsh-Hadamard fold: A_g <- A_g R, B_g <- R^T B_g
+    (Palu notes, "方法细节", Hadamard paragraph).
+  * Latents H = x A with x ~ N(0, I_d). For large workloads the equivalent draw
+    H = z sqrt(S_r) [R] with z ~ N(0, I_r) is used: x U_r is exactly N(0, I_r)
+    because U_r has orthonormal columns, so the latents have the same
+    distribution (K and V latents are then drawn independently).
+  * q ~ N(0, I) per head; positions 0..T-1.
+Seeds: numpy PCG64 streams spawned from SeedSequence(20261202 + config id), one
+each for W_k, W_v, x, q and W_o.
+"""
+from __future__ import annotations
+
+import dataclasses
+import functools
+import math
+
+import numpy as np
+import scipy.linalg
+
+SEED_BASE = 20261202
+# Above this many activation elements (B*T*d) the equivalent latent draw is used.
+EXACT_X_LIMIT = 1 << 26
+
+
+@dataclasses.dataclass(frozen=True)
+class Config:
+    cid: int
+    name: str
+    batch: int
+    n_heads: int
+    head_dim: int
+    hidden: int
+    group_size: int
+    rank: int            # r_k = r_v = r_g
+    T: int
+    latent_dtype: str    # "f32" | "f16" | "bf16" | "int4"
+    mode: str            # "rope" | "absorbed"
+    sigma_tau: float     # sigma_i = exp(-i / tau)
+    hadamard: bool = False
+    theta: float = 10000.0
+
+    @property
+    def n_groups(self) -> int:
+        return self.n_heads // self.group_size
+
+    @property
+    def bk_dtype(self) -> str:
+        # int4 latents are dequantised to fp16 before the rebuild contraction
+        return "f16" if self.latent_dtype == "int4" else self.latent_dtype
+
+    @property
+    def q_dtype(self) -> str:
+        return self.bk_dtype
+
+    def with_(self, **kw) -> "Config":
+        return dataclasses.replace(self, **kw)
+
+
+CONFIGS = {
+    1: Config(1, "tiny-fp32", 1, 8, 64, 512, 4, 128, 512, "f32", "rope", 64.0),
+    2: Config(2, "llama2-7b-rope-fp16", 1, 32, 128, 4096, 4, 256, 4096, "f16", "rope", 512.0),
+    3: Config(3, "llama2-7b-rope-bf16", 8, 32, 128, 4096, 4, 256, 32768, "bf16", "rope", 512.0),
+    4: Config(4, "llama2-7b-absorbed-fp16", 4, 32, 128, 4096, 4, 256, 65536, "f16", "absorbed", 512.0),
+    5: Config(5, "llama2-7b-rope-int4-hadamard", 4, 32, 128, 4096, 4, 256, 65536, "int4", "rope", 512.0,
+              hadamard=True),
+}
+
+
+def config_by_id(cid: int, **overrides) -> Config:
+    c = CONFIGS[cid]
+    return c.with_(**overrides) if overrides else c
+
+
+def _streams(cid: int):
+    ss = np.random.SeedSequence(SEED_BASE + cid)
+    return [np.random.Generator(np.random.PCG64(s)) for s in ss.spawn(5)]
+
+
+def _haar(rng: np.random.Generator, n: int) -> np.ndarray:
+    z = rng.standard_normal((n, n))
+    q, r = np.linalg.qr(z)
+    return q * np.sign(np.diag(r))[None, :]
+
+
+@functools.lru_cache(maxsize=8)
+def _weights(cid: int, hidden: int, tau: float):
+    """Spectrum-decay W_k, W_v (hidden x hidden), float64."""
+    rk, rv, _, _, _ = _streams(cid)
+    sig = np.exp(-np.arange(hidden) / tau)
+    out = []
+    for rng in (rk, rv):
+        u = _haar(rng, hidden)
+        v = _haar(rng, hidden)
+        out.append((u * sig[None, :]) @ v.T)
+    return out[0], out[1]
+
+
+@functools.lru_cache(maxsize=8)
+def _factors(cfg_key):
+    cid, hidden, tau, n_g, s, d_h, r, had = cfg_key
+    wk, wv = _weights(cid, hidden, tau)
+    R = scipy.linalg.hadamard(r).astype(np.float64) / math.sqrt(r) if had else None
+    res = {}
+    for name, w in (("k", wk), ("v", wv)):
+        A = np.empty((n_g, hidden, r))
+        B = np.empty((n_g, r, s * d_h))
+        S_all = np.empty((n_g, r))
+        for g in range(n_g):
+            wg = w[:, g * s * d_h:(g + 1) * s * d_h]
+            u, sv, vt = np.linalg.svd(wg, full_matrices=False)
+            rs = np.sqrt(sv[:r])
+            A[g] = u[:, :r] * rs[None, :]
+            B[g] = rs[:, None] * vt[:r]
+            S_all[g] = sv[:r]
+            if R is not None:
+                A[g] = A[g] @ R
+                B[g] = R.T @ B[g]
+        res[name] = (A, B, S_all)
+    return res, R
+
+
+def weights(cfg: Config):
+    """(W_k, W_v) float64 full projection matrices of the configuration."""
+    return _weights(cfg.cid, cfg.hidden, cfg.sigma_tau)
+
+
+def factors(cfg: Config):
+    key = (cfg.cid, cfg.hidden, cfg.sigma_tau, cfg.n_groups, cfg.group_size, cfg.head_dim,
+           cfg.rank, cfg.hadamard)
+    return _factors(key)
+
+
+def make_inputs(cfg: Config, *, exact_x: bool | None = None, q_scale: float = 1.0,
+                with_x: bool = False, with_wo: bool = False) -> dict:
+    """Draw one workload. Returns float32/float64 numpy arrays (unrounded):
+
+    hk, hv : [B][T][n_g][r] float32 latents (cache layout)
+    bk, bv : [n_g][r][s*d_h] float64 reconstruction factors (Hadamard-folded if set)
+    ak, av : [n_g][d][r] float64 down-projections
+    q      : [B][n][d_h] float32 query (not rotated)
+    x      : [B][T][d] float32 activations (only when drawn exactly and with_x)
+    wo     : [d][d] float64 output projection ~ N(0, 1/d) (only with with_wo)
+    """
+    B, T, d = cfg.batch, cfg.T, cfg.hidden
+    n_g, r, s, d_h = cfg.n_groups, cfg.rank, cfg.group_size, cfg.head_dim
+    fac, R = factors(cfg)
+    _, _, rx, rq, ro = _streams(cfg.cid)
+    if exact_x is None:
+        exact_x = B * T * d <= EXACT_X_LIMIT
+    out = {"cfg": cfg}
+    if exact_x:
+        x = rx.standard_normal((B, T, d), dtype=np.float32)
+        ak = fac["k"][0].astype(np.float32)
+        av = fac["v"][0].astype(np.float32)
+        hk = np.einsum("btd,gdr->btgr", x, ak, optimize=True).astype(np.float32)
+        hv = np.einsum("btd,gdr->btgr", x, av, optimize=True).astype(np.float32)
+        if with_x:
+            out["x"] = x
+    else:
+        hk = np.empty((B, T, n_g, r), np.float32)
+        hv = np.empty((B, T, n_g, r), np.float32)
+        for h, name in ((hk, "k"), (hv, "v")):
+            sq = np.sqrt(fac[name][2]).astype(np.float32)       # [n_g][r]
+            Rf = None if R is None else R.astype(np.float32)
+            for b in range(B):
+                z = rx.standard_normal((T, n_g, r), dtype=np.float32)
+                z *= sq[None, :, :]
+                if Rf is not None:
+                    z = z @ Rf
+                h[b] = z
+    out["hk"], out["hv"] = hk, hv
+    out["bk"], out["bv"] = fac["k"][1], fac["v"][1]
+    out["ak"], out["av"] = fac["k"][0], fac["v"][0]
+    out["sk"], out["sv"] = fac["k"][2], fac["v"][2]
+    q = rq.standard_normal((B, cfg.n_heads, d_h), dtype=np.float32)
+    out["q"] = q * np.float32(q_scale)
+    if with_wo:
+        out["wo"] = ro.standard_normal((d, d)) / math.sqrt(d)
+    out["R"] = R
+    return out
+
+
+_TORCH_DT = {"f32": "float32", "f16": "float16", "bf16": "bfloat16"}
+
+
+def storage_round(a, dtype: str):
+    """Round an array to a storage dtype ("f32"/"f16"/"bf16"); returns a CPU torch tensor.
+
+    The rounded tensor is what both the CUDA path and the oracle consume (the
+    oracle upcasts it to float64), so rounding never separates the two sides.
+    """
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
+    return t.to(getattr(torch, _TORCH_DT[dtype]))
+
+
+def hadamard_sylvester(r: int) -> np.ndarray:
+    """Normalised Sylvester Walsh-Hadamard matrix (input preparation only)."""
+    return scipy.linalg.hadamard(r).astype(np.float64) / math.sqrt(r)

@@ -1,0 +1,138 @@
+"""Plant plausible mistakes in the oracle (CPU only) and check the pins catch each.
+
+Every mutation below is a realistic slip: wrong rotation sign, wrong pairing,
+wrong frequency schedule, wrong head-to-group map, wrong score scale, wrong
+rounding mode, swapped nibbles. The pin tests must fail on each one.
+"""
+import math
+
+import numpy as np
+import pytest
+
+from oracle import palu_oracle as O
+from tests import test_oracle_pins as P
+
+
+def _rope_wrong_sign(x, pos, theta):
+    x = np.asarray(x, np.float64)
+    d = x.shape[-1]
+    ang = np.asarray(pos, np.float64)[..., None] * O.rope_inv_freq(d, theta)
+    c, s = np.cos(ang), np.sin(ang)
+    a, b = x[..., :d // 2], x[..., d // 2:]
+    return np.concatenate([a * c + b * s, b * c - a * s], axis=-1)
+
+
+def _rope_interleaved(x, pos, theta):
+    x = np.asarray(x, np.float64)
+    d = x.shape[-1]
+    ang = np.asarray(pos, np.float64)[..., None] * O.rope_inv_freq(d, theta)
+    c, s = np.cos(ang), np.sin(ang)
+    a, b = x[..., 0::2], x[..., 1::2]
+    out = np.empty(np.broadcast_shapes(x.shape, ang.shape[:-1] + (d,)))
+    out[..., 0::2] = a * c - b * s
+    out[..., 1::2] = b * c + a * s
+    return out
+
+
+def _inv_freq_half(head_dim, theta):
+    k = np.arange(head_dim // 2, dtype=np.float64)
+    return np.power(float(theta), -k / head_dim)
+
+
+def _group_of_modulo(head, group_size):
+    # heads strided across groups instead of consecutive
+    return head % group_size, head // group_size
+
+
+def _rope_head_scale_r(q_i, hk_bg, hv_bg, bk_g, j, pos, qp, theta):
+    d_h = q_i.shape[-1]
+    r = hk_bg.shape[-1]
+    K = hk_bg @ bk_g[:, j * d_h:(j + 1) * d_h]
+    s = (O.rope_rotate(K, pos, theta) @ O.rope_rotate(q_i, qp, theta)) / math.sqrt(r)
+    return O.softmax_attend(s, hv_bg)
+
+
+def _absorbed_transposed(q_i, hk_bg, hv_bg, bk_g, j):
+    # uses the head's row block of B^T instead of its column block of B
+    d_h = q_i.shape[-1]
+    blk = bk_g[:, j * d_h:(j + 1) * d_h]
+    q_lat = np.zeros(bk_g.shape[0])
+    q_lat[:d_h] = blk[:d_h, :] @ q_i
+    return O.softmax_attend(hk_bg @ q_lat / math.sqrt(d_h), hv_bg)
+
+
+def _quantize_half_away(h):
+    h = np.asarray(h, np.float32)
+    amax = np.max(np.abs(h), axis=-1)
+    scale = np.minimum(amax / np.float32(7), np.float32(O.FP16_MAX)).astype(np.float16)
+    sf = scale.astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = h / sf[..., None]
+    codes = np.clip(np.sign(r) * np.floor(np.abs(r) + 0.5), -7, 7)
+    return np.where((sf == 0)[..., None], 0, codes).astype(np.int8), scale
+
+
+def _pack_swapped(codes):
+    c = np.asarray(codes, np.int16) & 0xF
+    return (c[..., 1::2] | (c[..., 0::2] << 4)).astype(np.uint8)
+
+
+def _qpos_off_by_one(positions, q_pos, b, T):
+    if q_pos is not None:
+        return float(q_pos[b])
+    return float(T) if positions is None else float(positions[b][T - 1]) + 1
+
+
+def _softmax_no_norm(scores, values):
+    scores = np.asarray(scores, np.float64)
+    if scores.size == 0:
+        return np.zeros(values.shape[-1]), -math.inf
+    m = scores.max()
+    e = np.exp(scores - m)
+    return e @ values, m + math.log(e.sum())
+
+
+ALL_PINS = [getattr(P, n) for n in dir(P) if n.startswith("test_")]
+
+MUTATIONS = {
+    "rope_wrong_sign": ("rope_rotate", _rope_wrong_sign),
+    "rope_interleaved_pairs": ("rope_rotate", _rope_interleaved),
+    "rope_frequency_schedule": ("rope_inv_freq", _inv_freq_half),
+    "head_group_map": ("_group_of", _group_of_modulo),
+    "score_scale_sqrt_r": ("decode_rope_head", _rope_head_scale_r),
+    "absorbed_transposed_block": ("decode_absorbed_head", _absorbed_transposed),
+    "int4_round_half_away": ("quantize_int4", _quantize_half_away),
+    "int4_nibble_order": ("pack_int4", _pack_swapped),
+    "query_position_default": ("_query_position", _qpos_off_by_one),
+    "softmax_unnormalised": ("softmax_attend", _softmax_no_norm),
+}
+
+
+def _run_pins(pins):
+    failed = []
+    for fn in pins:
+        params = getattr(fn, "pytestmark", [])
+        arglists = [{}]
+        for m in params:
+            if m.name == "parametrize":
+                name, vals = m.args[0], m.args[1]
+                arglists = [{name: v} for v in vals]
+        for kw in arglists:
+            try:
+                fn(**kw)
+            except (AssertionError, ValueError, IndexError):
+                failed.append(fn.__name__)
+                break
+    return failed
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_planted_mistake(name, monkeypatch):
+    attr, mutant = MUTATIONS[name]
+    monkeypatch.setattr(O, attr, mutant)
+    failed = _run_pins(ALL_PINS)
+    assert failed, f"no pin caught the planted mistake {name}"
+
+
+def test_unmutated_oracle_passes_every_pin():
+    assert _run_pins(ALL_PINS) == []

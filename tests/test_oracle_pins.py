@@ -1,0 +1,369 @@
+"""CPU pins for the float64 oracle.
+
+Each test ties an oracle function to something other than itself: a closed
+form, a worked number printed on the pages, a library routine, an identity the
+pages derive, or a pure-Python brute force on tiny inputs.
+"""
+import cmath
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.linalg
+import scipy.special
+
+from oracle import palu_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------------------
+# RoPE
+# ---------------------------------------------------------------------------
+
+def test_rope_two_dims_is_plane_rotation_by_position_radians():
+    # d_h = 2: one pair with omega_0 = theta^0 = 1, so position p rotates by p radians.
+    for p in (0.0, 1.0, 2.5, 100.0):
+        out = O.rope_rotate(np.array([1.0, 0.0]), p, 10000.0)
+        np.testing.assert_allclose(out, [math.cos(p), math.sin(p)], atol=1e-15)
+        out = O.rope_rotate(np.array([0.0, 1.0]), p, 10000.0)
+        np.testing.assert_allclose(out, [-math.sin(p), math.cos(p)], atol=1e-15)
+
+
+def test_rope_frequencies_closed_form():
+    # d_h = 4, theta = 10000: omega = [1, 10000^(-1/2)] = [1, 0.01].
+    np.testing.assert_allclose(O.rope_inv_freq(4, 10000.0), [1.0, 0.01], rtol=1e-15)
+    # last pair of d_h = 128 at theta = 10000: 10000^(-126/128)
+    w = O.rope_inv_freq(128, 10000.0)
+    assert w[0] == 1.0 and abs(w[-1] - 10000.0 ** (-126 / 128)) < 1e-18
+    assert np.all(np.diff(w) < 0)
+
+
+def test_rope_undone_by_shard_inverse_formula():
+    # Shard section 5 step 1: k_no_rope = k*cos(theta p) - rotate_half(k)*sin(theta p),
+    # rotate_half([a, b]) = [-b, a]. It must undo the oracle's forward rotation.
+    rng = np.random.default_rng(0)
+    d = 16
+    x = rng.standard_normal((5, d))
+    pos = np.array([0, 1, 7, 300, 65535], dtype=np.float64)
+    y = O.rope_rotate(x, pos, 10000.0)
+    k = np.arange(d // 2)
+    ang = pos[:, None] * (10000.0 ** (-2.0 * k / d))[None, :]
+    cos = np.concatenate([np.cos(ang)] * 2, axis=1)
+    sin = np.concatenate([np.sin(ang)] * 2, axis=1)
+    rot_half = np.concatenate([-y[:, d // 2:], y[:, :d // 2]], axis=1)
+    x_back = y * cos - rot_half * sin
+    np.testing.assert_allclose(x_back, x, atol=1e-12)
+
+
+def test_rope_identity_at_zero_norm_preserving_and_relative():
+    rng = np.random.default_rng(1)
+    d = 32
+    x = rng.standard_normal(d)
+    np.testing.assert_array_equal(O.rope_rotate(x, 0.0, 10000.0), x)
+    for p in (1, 17, 4095, 65535):
+        np.testing.assert_allclose(np.linalg.norm(O.rope_rotate(x, p, 1e4)), np.linalg.norm(x), rtol=1e-13)
+    # scores depend only on the relative position (RoFormer property)
+    q = rng.standard_normal(d)
+    k = rng.standard_normal(d)
+    base = O.rope_rotate(q, 100, 1e4) @ O.rope_rotate(k, 37, 1e4)
+    for c in (1, 5, 1000):
+        sh = O.rope_rotate(q, 100 + c, 1e4) @ O.rope_rotate(k, 37 + c, 1e4)
+        assert abs(sh - base) < 1e-10
+
+
+# ---------------------------------------------------------------------------
+# Softmax / attention
+# ---------------------------------------------------------------------------
+
+def test_softmax_attend_matches_scipy():
+    rng = np.random.default_rng(2)
+    s = rng.standard_normal(50) * 3
+    v = rng.standard_normal((50, 7))
+    o, lse = O.softmax_attend(s, v)
+    np.testing.assert_allclose(o, scipy.special.softmax(s) @ v, rtol=1e-13)
+    assert abs(lse - scipy.special.logsumexp(s)) < 1e-12
+
+
+def _tiny(seed=3, B=2, T=6, n=4, s=2, d_h=4, r=4, r_v=3):
+    rng = np.random.default_rng(seed)
+    n_g = n // s
+    q = rng.standard_normal((B, n, d_h))
+    hk = rng.standard_normal((B, T, n_g, r))
+    hv = rng.standard_normal((B, T, n_g, r_v))
+    bk = rng.standard_normal((n_g, r, s * d_h))
+    return q, hk, hv, bk
+
+
+def test_single_token_returns_its_value_latent():
+    q, hk, hv, bk = _tiny(T=1)
+    for mode in ("rope", "absorbed"):
+        o, lse = O.decode(q, hk, hv, bk, [1, 1], 2, mode=mode)
+        for b in range(2):
+            for i in range(4):
+                np.testing.assert_allclose(o[b, i], hv[b, 0, i // 2], rtol=1e-14)
+
+
+def test_zero_query_is_mean_of_values_and_lse_log_T():
+    q, hk, hv, bk = _tiny(T=6)
+    q[:] = 0
+    for mode in ("rope", "absorbed"):
+        o, lse = O.decode(q, hk, hv, bk, [6, 4], 2, mode=mode)
+        np.testing.assert_allclose(o[0, 1], hv[0, :6, 0].mean(axis=0), rtol=1e-13)
+        np.testing.assert_allclose(o[1, 3], hv[1, :4, 1].mean(axis=0), rtol=1e-13)
+        np.testing.assert_allclose(lse[0], math.log(6), rtol=1e-14)
+        np.testing.assert_allclose(lse[1], math.log(4), rtol=1e-14)
+
+
+def test_equal_key_latents_give_uniform_weights_absorbed():
+    q, hk, hv, bk = _tiny(T=5)
+    hk[:] = hk[:, :1]
+    o, _ = O.decode(q, hk, hv, bk, [5, 5], 2, mode="absorbed")
+    np.testing.assert_allclose(o[1, 2], hv[1, :, 1].mean(axis=0), rtol=1e-13)
+
+
+def test_empty_sequence():
+    q, hk, hv, bk = _tiny(T=3)
+    o, lse = O.decode(q, hk, hv, bk, [0, 3], 2)
+    assert np.all(o[0] == 0) and np.all(np.isneginf(lse[0]))
+    assert np.all(np.isfinite(lse[1]))
+
+
+# ---------------------------------------------------------------------------
+# Brute force on tiny inputs: scalar loops, math.fsum, complex-number rotation
+# ---------------------------------------------------------------------------
+
+def _brute_rope_decode(q, hk, hv, bk, T, s, theta, pos, qp):
+    n, d_h = len(q), len(q[0])
+    half = d_h // 2
+
+    def rot(vec, p):
+        out = [0.0] * d_h
+        for c in range(half):
+            z = complex(vec[c], vec[c + half]) * cmath.exp(1j * p * theta ** (-(2 * c) / d_h))
+            out[c], out[c + half] = z.real, z.imag
+        return out
+
+    res = []
+    for i in range(n):
+        g, j = i // s, i % s
+        qr = rot(list(q[i]), qp)
+        scores = []
+        for t in range(T):
+            k = [math.fsum(hk[t][g][m] * bk[g][m][j * d_h + c] for m in range(len(bk[g])))
+                 for c in range(d_h)]
+            kr = rot(k, pos[t])
+            scores.append(math.fsum(a * b for a, b in zip(qr, kr)) / math.sqrt(d_h))
+        mx = max(scores)
+        e = [math.exp(x - mx) for x in scores]
+        l = math.fsum(e)
+        o = [math.fsum(e[t] * hv[t][g][m] for t in range(T)) / l for m in range(len(hv[0][g]))]
+        res.append((o, mx + math.log(l)))
+    return res
+
+
+def test_brute_force_rope_tiny():
+    q, hk, hv, bk = _tiny(seed=4, B=2, T=7, n=4, s=2, d_h=4, r=4, r_v=3)
+    pos = np.array([[3, 9, 1, 0, 22, 5, 6], [0, 1, 2, 3, 4, 5, 6]])
+    qp = np.array([30, 6])
+    theta = 100.0
+    o, lse = O.decode(q, hk, hv, bk, [7, 5], 2, mode="rope", theta=theta, positions=pos, q_pos=qp)
+    for b, T in ((0, 7), (1, 5)):
+        ref = _brute_rope_decode(q[b].tolist(), hk[b].tolist(), hv[b].tolist(), bk.tolist(), T, 2,
+                                 theta, pos[b].tolist(), float(qp[b]))
+        for i, (ro, rl) in enumerate(ref):
+            np.testing.assert_allclose(o[b, i], ro, rtol=1e-12, atol=1e-13)
+            assert abs(lse[b, i] - rl) < 1e-12
+
+
+def test_default_query_position_is_last_cached_token():
+    q, hk, hv, bk = _tiny(seed=5, T=6)
+    pos = np.array([[4, 8, 15, 16, 23, 42], [1, 2, 3, 5, 8, 13]])
+    a = O.decode(q, hk, hv, bk, [6, 4], 2, positions=pos)
+    b = O.decode(q, hk, hv, bk, [6, 4], 2, positions=pos, q_pos=[42, 5])
+    np.testing.assert_array_equal(a[0], b[0])
+    c = O.decode(q, hk, hv, bk, [6, 4], 2)
+    d = O.decode(q, hk, hv, bk, [6, 4], 2, q_pos=[5, 3])
+    np.testing.assert_array_equal(c[0], d[0])
+
+
+# ---------------------------------------------------------------------------
+# Identities the Palu notes derive
+# ---------------------------------------------------------------------------
+
+def _mha_setup(seed, B=2, T=9, d=64, n=4, s=2, d_h=8):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((B, T, d))
+    wk = rng.standard_normal((d, n * d_h)) / math.sqrt(d)
+    wv = rng.standard_normal((d, n * d_h)) / math.sqrt(d)
+    q = rng.standard_normal((B, n, d_h))
+    return x, wk, wv, q
+
+
+def _group_factors(w, n_g, s, d_h, r):
+    A, B = [], []
+    for g in range(n_g):
+        a, b = O.svd_factor(w[:, g * s * d_h:(g + 1) * s * d_h], r)
+        A.append(a)
+        B.append(b)
+    return np.stack(A), np.stack(B)
+
+
+@pytest.mark.parametrize("mode", ["rope", "absorbed"])
+def test_full_rank_latent_decode_equals_uncompressed_mha(mode):
+    # With r = s*d_h the group factors are exact, so decode over latents must be MHA.
+    B, T, d, n, s, d_h = 2, 9, 64, 4, 2, 8
+    x, wk, wv, q = _mha_setup(6, B, T, d, n, s, d_h)
+    n_g, r = n // s, s * d_h
+    Ak, Bk = _group_factors(wk, n_g, s, d_h, r)
+    Av, Bv = _group_factors(wv, n_g, s, d_h, r)
+    hk = np.einsum("btd,gdr->btgr", x, Ak)
+    hv = np.einsum("btd,gdr->btgr", x, Av)
+    seq = [9, 6]
+    pos = np.array([[5, 1, 2, 9, 4, 7, 3, 0, 8], list(range(9))])
+    o, lse = O.decode(q, hk, hv, Bk, seq, s, mode=mode, positions=pos, q_pos=[11, 5])
+    a, lse_ref = O.mha_decode(q, x, wk, wv, seq, rope=(mode == "rope"), positions=pos, q_pos=[11, 5])
+    for b in range(B):
+        for i in range(n):
+            g, j = i // s, i % s
+            np.testing.assert_allclose(o[b, i] @ Bv[g][:, j * d_h:(j + 1) * d_h], a[b, i], atol=1e-11)
+    np.testing.assert_allclose(lse, lse_ref, atol=1e-11)
+
+
+def test_value_fusion_into_output_projection():
+    # p H_v (B_v W_o) == (p V) W_o with V = H_v B_v, at truncated rank.
+    B, T, d, n, s, d_h, r = 1, 12, 64, 4, 2, 8, 5
+    x, wk, wv, q = _mha_setup(7, B, T, d, n, s, d_h)
+    rng = np.random.default_rng(8)
+    wo = rng.standard_normal((n * d_h, d)) / math.sqrt(d)
+    n_g = n // s
+    Ak, Bk = _group_factors(wk, n_g, s, d_h, r)
+    Av, Bv = _group_factors(wv, n_g, s, d_h, r)
+    hk = np.einsum("btd,gdr->btgr", x, Ak)
+    hv = np.einsum("btd,gdr->btgr", x, Av)
+    o, _ = O.decode(q, hk, hv, Bk, [T], s)
+    # uncompressed MHA with the low-rank weights W' = A B (block columns per group)
+    wk_lr = np.concatenate([Ak[g] @ Bk[g] for g in range(n_g)], axis=1)
+    wv_lr = np.concatenate([Av[g] @ Bv[g] for g in range(n_g)], axis=1)
+    a, _ = O.mha_decode(q, x, wk_lr, wv_lr, [T])
+    y_ref = sum(a[0, i] @ wo[i * d_h:(i + 1) * d_h] for i in range(n))
+    y = sum(o[0, i] @ (Bv[i // s][:, (i % s) * d_h:(i % s + 1) * d_h] @ wo[i * d_h:(i + 1) * d_h])
+            for i in range(n))
+    np.testing.assert_allclose(y, y_ref, atol=1e-11)
+
+
+def test_absorbed_equals_rebuild_when_rotation_is_identity():
+    # Key fusion: q K^T = (q B^T) H^T. With every position 0, RoPE is the identity.
+    q, hk, hv, bk = _tiny(seed=9, B=2, T=8, n=4, s=2, d_h=4, r=4, r_v=3)
+    zeros = np.zeros((2, 8), dtype=np.int64)
+    a = O.decode(q, hk, hv, bk, [8, 3], 2, mode="rope", positions=zeros, q_pos=[0, 0])
+    b = O.decode(q, hk, hv, bk, [8, 3], 2, mode="absorbed")
+    np.testing.assert_allclose(a[0], b[0], atol=1e-13)
+    np.testing.assert_allclose(a[1], b[1], atol=1e-13)
+
+
+# ---------------------------------------------------------------------------
+# SVD factors and the Hadamard fold
+# ---------------------------------------------------------------------------
+
+def test_svd_factor_eckart_young_and_balanced_split():
+    rng = np.random.default_rng(10)
+    w = rng.standard_normal((40, 24))
+    sv = np.linalg.svd(w, compute_uv=False)
+    for r in (1, 5, 24):
+        A, B = O.svd_factor(w, r)
+        assert A.shape == (40, r) and B.shape == (r, 24)
+        err = np.linalg.norm(w - A @ B) ** 2
+        assert abs(err - np.sum(sv[r:] ** 2)) < 1e-9
+        # A = U_r sqrt(S_r), B = sqrt(S_r) V_r^T  =>  A^T A = B B^T = diag(S_r)
+        np.testing.assert_allclose(A.T @ A, np.diag(sv[:r]), atol=1e-10)
+        np.testing.assert_allclose(B @ B.T, np.diag(sv[:r]), atol=1e-10)
+
+
+def test_hadamard_matches_scipy_and_is_orthogonal():
+    for r in (1, 2, 8, 16, 128, 256):
+        R = O.hadamard(r)
+        np.testing.assert_array_equal(R, scipy.linalg.hadamard(r) / math.sqrt(r))
+        if r in (1, 16, 256):  # 1/sqrt(r) is a power of two: R R^T = I exactly
+            np.testing.assert_array_equal(R @ R.T, np.eye(r))
+        else:
+            np.testing.assert_allclose(R @ R.T, np.eye(r), atol=1e-15)
+    R = O.hadamard(256)
+    assert set(np.unique(R)) == {-1 / 16, 1 / 16}
+
+
+def test_hadamard_fold_preserves_product():
+    rng = np.random.default_rng(11)
+    A = rng.standard_normal((64, 16))
+    B = rng.standard_normal((16, 32))
+    R = O.hadamard(16)
+    np.testing.assert_allclose((A @ R) @ (R.T @ B), A @ B, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# int4 quantisation
+# ---------------------------------------------------------------------------
+
+def _read_int4_golden():
+    cases, cur = [], {}
+    with open(os.path.join(GOLDEN, "int4_pack.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, *vals = line.split()
+            cur[key] = vals
+            if key == "bytes":
+                cases.append(cur)
+                cur = {}
+    return cases
+
+
+def test_int4_golden_codes_and_bytes():
+    cases = _read_int4_golden()
+    assert len(cases) == 5
+    for c in cases:
+        h = np.array([float(v) for v in c["h"]], dtype=np.float32)[None]
+        codes, scale = O.quantize_int4(h)
+        assert scale.view(np.uint16)[0] == int(c["scale"][0], 16)
+        np.testing.assert_array_equal(codes[0], [int(v) for v in c["codes"]])
+        packed = O.pack_int4(codes)
+        np.testing.assert_array_equal(packed[0], [int(v, 16) for v in c["bytes"]])
+        np.testing.assert_array_equal(O.unpack_int4(packed), codes)
+
+
+def test_int4_properties():
+    rng = np.random.default_rng(12)
+    h = (rng.standard_normal((64, 256)) * rng.uniform(0.01, 30, (64, 1))).astype(np.float32)
+    codes, scale = O.quantize_int4(h)
+    assert codes.min() >= -7 and codes.max() <= 7
+    sf = scale.astype(np.float64)
+    deq = O.dequant_int4(O.pack_int4(codes), scale)
+    # dequantised value is the exact product (<= 4 + 11 significant bits)
+    np.testing.assert_array_equal(deq, codes.astype(np.float64) * sf[:, None])
+    np.testing.assert_array_equal(deq.astype(np.float32).astype(np.float64), deq)
+    # rounding error bounded by half a step where nothing is clamped
+    inside = np.abs(h / sf[:, None]) <= 7
+    assert np.all(np.abs(h - deq)[inside] <= sf[:, None].repeat(256, 1)[inside] / 2 * (1 + 1e-6))
+    # the largest-magnitude element maps to +-7 (scale rounding never pushes it below 6.5)
+    idx = np.argmax(np.abs(h), axis=1)
+    assert np.all(np.abs(codes[np.arange(64), idx]) == 7)
+
+
+def test_int4_integer_inputs_round_trip():
+    rng = np.random.default_rng(13)
+    codes_in = rng.integers(-7, 8, (32, 64)).astype(np.float32)
+    codes_in[:, 0] = 7  # amax 7 -> scale exactly 1
+    codes, scale = O.quantize_int4(codes_in)
+    assert np.all(scale == 1.0)
+    np.testing.assert_array_equal(codes, codes_in.astype(np.int8))
+    np.testing.assert_array_equal(O.dequant_int4(O.pack_int4(codes), scale), codes_in)
+
+
+def test_int4_huge_and_zero_rows():
+    h = np.zeros((2, 8), np.float32)
+    h[1] = 1e6
+    codes, scale = O.quantize_int4(h)
+    assert scale[0] == 0 and np.all(codes[0] == 0)
+    assert scale[1] == np.float16(65504.0) and np.all(codes[1] == 7)
