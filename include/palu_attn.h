@@ -1,0 +1,211 @@
+/*
+ * palu_attn.h -- C ABI for Palu-style group-head low-rank (G-LRD) decode
+ * attention over a latent KV cache, on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation ("Palu: KV-Cache Compression With Low-Rank Projection", method
+ * section "方法细节"):
+ *   - The key/value projections of each group of s consecutive heads are
+ *     factored offline, W_g ~= A_g B_g (truncated SVD, "背景知识"), and only the
+ *     latents h_g = x A_g (r values per token and group) are cached.
+ *   - RoPE models: each head's keys are rebuilt on chip from the cached latents,
+ *     K = H_k,g B_k,g[:, head block], rotated by RoPE at every token's own
+ *     position, and scored against the rotated query (RoPE paragraph and the
+ *     online-rebuild kernel paragraph of "补充细节").
+ *   - Non-RoPE models: the query is absorbed, q' = q B_k^T, and scored straight
+ *     against H_k (key-fusion paragraph).
+ *   - Softmax over all cached tokens, then p is applied to the value latents,
+ *     o = p H_v, so the output stays in latent space: B_v is fused into W_o
+ *     offline (value-fusion paragraph).
+ *   - Optionally the latents are stored as per-token int4 codes with an fp16
+ *     scale; a Walsh-Hadamard rotation folded into A and B beforehand needs no
+ *     run-time work (Hadamard paragraph).
+ *
+ * Conventions fixed by this library (the pages leave them open):
+ *   - Row vectors: h = x A, A in R^{d x r}. Head i is column block (i % s) of
+ *     group (i / s).
+ *   - Score scale 1/sqrt(d_h) on both paths.
+ *   - RoPE is rotate-half: pairs (k, k + d_h/2) rotated by pos * theta^(-2k/d_h).
+ *   - The query is passed UNROTATED; it is rotated at q_pos, which defaults to
+ *     the position of the last cached token. No causal mask.
+ *   - int4 codes: symmetric in [-7, 7], one fp16 scale per token and group,
+ *     scale = fp16_rn(min(amax / 7, 65504)) with IEEE fp32 division,
+ *     code = rint_half_even(h / scale) clamped to [-7, 7]; element 2j in the low
+ *     nibble and 2j+1 in the high nibble of byte j (two's complement).
+ *
+ * Memory: every pointer argument that the comments call "device" is device
+ * memory owned by the caller, and must stay valid until the work queued on the
+ * given stream has finished. The library allocates no device memory: scratch
+ * lives in the caller-provided workspace. A handle owns host memory only.
+ *
+ * Errors: every call returns a palu_status_t; nothing aborts, prints or throws.
+ * Argument checks happen on the host before anything is queued. Conditions only
+ * the GPU can see (a position outside the RoPE table, a sequence longer than
+ * the cache, a bounded wait that gave up) are recorded in an error word inside
+ * the workspace; the kernels clamp the offending index and carry on, and
+ * palu_attn_check reports (and clears) it. No other call synchronises.
+ *
+ * Threading: calls on one handle must not overlap (they share one workspace).
+ * Different handles are independent.
+ */
+#ifndef PALU_ATTN_H
+#define PALU_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PALU_ABI_VERSION 1
+
+/* A CUDA stream. Pass a cudaStream_t (or CUstream); NULL is the legacy default stream. */
+typedef struct CUstream_st* palu_stream_t;
+
+typedef enum palu_status_t {
+  PALU_OK = 0,
+  PALU_ERR_INVALID_ARG = 1,  /* null / misaligned pointer, bad size, inconsistent descriptor */
+  PALU_ERR_UNSUPPORTED = 2,  /* a valid shape or dtype combination this build has no kernel for */
+  PALU_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
+  PALU_ERR_DEVICE = 4,       /* a kernel recorded an out-of-range index in the error word */
+  PALU_ERR_TIMEOUT = 5,      /* a bounded device-side wait gave up (error word) */
+  PALU_ERR_WORKSPACE = 6     /* workspace missing, too small or not 256-byte aligned */
+} palu_status_t;
+
+typedef enum palu_dtype_t {
+  PALU_F32 = 0,
+  PALU_F16 = 1,
+  PALU_BF16 = 2,
+  PALU_INT4 = 3   /* latents only: packed codes + fp16 per-token scales */
+} palu_dtype_t;
+
+typedef enum palu_mode_t {
+  PALU_MODE_ROPE = 0,      /* rebuild K = H_k B_k on chip, rotate, score */
+  PALU_MODE_ABSORBED = 1   /* score q B_k^T straight against H_k (no RoPE) */
+} palu_mode_t;
+
+typedef struct palu_attn_desc {
+  int abi_version;        /* must be PALU_ABI_VERSION */
+  int n_heads;            /* n */
+  int head_dim;           /* d_h: 64 or 128 */
+  int group_size;         /* s: 1, 2, 4 or 8; n_heads % s == 0 */
+  int rank_k;             /* r_k per group: 64, 128 or 256 */
+  int rank_v;             /* r_v per group: 64, 128 or 256 */
+  palu_dtype_t k_dtype;   /* key-latent storage */
+  palu_dtype_t v_dtype;   /* value-latent storage; this build requires v_dtype == k_dtype */
+  palu_dtype_t bk_dtype;  /* B_k storage: equals k_dtype, or PALU_F16 when k_dtype is PALU_INT4 */
+  palu_dtype_t q_dtype;   /* query storage: F32, F16 or BF16 */
+  palu_mode_t mode;
+  double rope_theta;      /* RoPE base (e.g. 10000); ignored by the absorbed mode */
+  int max_batch;          /* largest batch any decode call will pass */
+  int64_t max_tokens;     /* largest sequence length any decode call will see */
+  int64_t max_position;   /* positions must lie in [0, max_position); 0 means max_tokens */
+  uint32_t flags;         /* reserved, must be 0 */
+} palu_attn_desc;
+
+/*
+ * A latent cache, caller-owned device memory. With n_g = n_heads / group_size:
+ *   hk       [max_rows][capacity][n_g][rank_k] elements of k_dtype
+ *            (PALU_INT4: [max_rows][capacity][n_g][rank_k / 2] bytes)
+ *   hv       [max_rows][capacity][n_g][rank_v] elements of v_dtype (same rule)
+ *   k_scale  PALU_INT4 only: [max_rows][capacity][n_g] fp16 scales, else NULL
+ *   v_scale  PALU_INT4 only: same for hv, else NULL
+ * Batch element b of a call uses row b. hk and hv must be 16-byte aligned.
+ */
+typedef struct palu_cache {
+  void* hk;
+  void* hv;
+  void* k_scale;
+  void* v_scale;
+  int64_t capacity;       /* tokens per row (the token stride) */
+} palu_cache;
+
+typedef struct palu_attn* palu_attn_t;
+
+/* Bytes of device workspace palu_attn_create needs for this descriptor. */
+palu_status_t palu_attn_workspace_size(const palu_attn_desc* desc, size_t* bytes);
+
+/*
+ * Create a handle. B_k is device memory [n_g][rank_k][group_size * head_dim]
+ * row-major in desc->bk_dtype: the per-group reconstruction factor B_g of the
+ * G-LRD factorisation ("方法细节", G-LRD paragraph), already Hadamard-folded if
+ * the latents were rotated. It is copied (and re-laid out) into the workspace
+ * on `stream`, together with a RoPE cos/sin table computed in float64, so B_k
+ * may be freed once that stream has passed this call. `workspace` (device,
+ * 256-byte aligned, at least palu_attn_workspace_size bytes) must outlive the
+ * handle. The handle itself is host memory.
+ */
+palu_status_t palu_attn_create(const palu_attn_desc* desc, const void* B_k, void* workspace,
+                               size_t workspace_bytes, palu_stream_t stream, palu_attn_t* out);
+
+/*
+ * Append n_new tokens per batch row to the cache ("方法细节": the latents h = x A
+ * are what is stored). hk_new [batch][n_new][n_g][rank_k] and hv_new
+ * [batch][n_new][n_g][rank_v] are device arrays of src_dtype (F32, F16 or BF16).
+ * dst_slot (device, [batch] int32) gives the first token index written in each
+ * row; tokens dst_slot[b] .. dst_slot[b] + n_new - 1 are overwritten. Float
+ * caches store the values rounded to nearest; int4 caches quantise them per
+ * token and group (convention in the file header). An index past the capacity
+ * is recorded in the error word and the row is skipped.
+ */
+palu_status_t palu_append_latents(palu_attn_t h, const palu_cache* cache, const void* hk_new,
+                                  const void* hv_new, palu_dtype_t src_dtype, const int32_t* dst_slot,
+                                  int batch, int n_new, palu_stream_t stream);
+
+/*
+ * Decode attention for one new query per batch row.
+ *   q          device [batch][n_heads][head_dim], desc->q_dtype, unrotated
+ *   seq_lens   device [batch] int32: tokens 0 .. seq_lens[b]-1 of row b attend
+ *   positions  device [batch][capacity] int32 RoPE positions, or NULL for
+ *              position = token index (ignored by the absorbed mode)
+ *   q_pos      device [batch] int32 query positions, or NULL for the position of
+ *              the last cached token (ignored by the absorbed mode)
+ *   max_seq_len host upper bound on every seq_lens[b] (<= desc->max_tokens and
+ *              <= cache->capacity); it sizes the launch. A larger seq_lens[b] is
+ *              clamped and recorded in the error word.
+ *   out        device [batch][n_heads][rank_v] float32: o_i = p_i H_v,g
+ *   lse        device [batch][n_heads] float32 natural log-sum-exp of the scaled
+ *              scores, or NULL. An empty row (seq_lens[b] == 0) yields o = 0 and
+ *              lse = -inf.
+ * Asynchronous on `stream`.
+ */
+palu_status_t palu_decode_attn(palu_attn_t h, const void* q, const palu_cache* cache,
+                               const int32_t* seq_lens, const int32_t* positions, const int32_t* q_pos,
+                               int batch, int64_t max_seq_len, float* out, float* lse,
+                               palu_stream_t stream);
+
+/* Free the host handle. Does not synchronise: no work on it may be in flight. NULL is fine. */
+palu_status_t palu_destroy(palu_attn_t h);
+
+/* Read and clear the device error word (synchronises `stream`). PALU_OK if nothing was recorded. */
+palu_status_t palu_attn_check(palu_attn_t h, palu_stream_t stream);
+
+/*
+ * Tracing. While enabled, every palu_decode_attn call records a pair of CUDA
+ * events around its main attention kernel, on the call's stream, into a ring of
+ * PALU_TRACE_CAPACITY pairs (the events are created by the library and hold no
+ * device memory; launches beyond the capacity are not recorded).
+ * palu_attn_trace_read waits for the recorded events, returns the number of
+ * recorded launches and their summed device time in milliseconds, and empties
+ * the ring. Disabling destroys the events.
+ */
+#define PALU_TRACE_CAPACITY 4096
+palu_status_t palu_attn_trace_enable(palu_attn_t h, int enable);
+palu_status_t palu_attn_trace_read(palu_attn_t h, int* launches, double* total_ms);
+
+/* Static description of a status code. */
+const char* palu_status_string(palu_status_t s);
+
+/*
+ * Test hook for the int4 load path: writes, as float32, the dequantised latents
+ * (code * scale) of tokens [0, n_tokens) of cache rows [0, batch) into
+ * out [batch][n_tokens][n_g][rank] (device), using the same unpack routine the
+ * decode kernels use. which = 0 for keys, 1 for values.
+ */
+palu_status_t palu_debug_dequant(palu_attn_t h, const palu_cache* cache, int which, int batch,
+                                 int64_t n_tokens, float* out, palu_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PALU_ATTN_H */

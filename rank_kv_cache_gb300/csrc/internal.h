@@ -1,0 +1,64 @@
+// Internal interface between the C ABI (palu_host.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace palu {
+
+// Everything a decode launch needs, flattened to plain pointers and sizes.
+struct DecodeArgs {
+  // latent cache
+  const void* hk;
+  const void* hv;
+  const __half* k_scale;
+  const __half* v_scale;
+  int64_t capacity;
+  // shapes and types
+  int n_heads, n_g, s, dh, rk, rv;
+  int k_dtype, v_dtype, bk_dtype;
+  // per call
+  const int32_t* seq_lens;
+  const int32_t* positions;   // nullable
+  int batch;
+  int max_seq_len;
+  int64_t max_pos;
+  // workspace-resident operands
+  const float* qbuf;          // [B][n][dh] rotated (rope) or [B][n][rk] absorbed; pre-scaled by log2(e)/sqrt(dh)
+  const void* bk;             // [n_g][rk][s*dh], bk_dtype
+  const void* bkt;            // [n_g][s*dh][rk], MMA dtype (K-major operand for tcgen05)
+  const float2* rope;         // [max_pos][dh/2] (cos, sin)
+  // split-T partials
+  float* part_o;              // [B][n][n_splits][rv]
+  float2* part_ml;            // [B][n][n_splits] (running max m in log2 units, sum l)
+  int n_splits;
+  int tiles_per_split;
+  ErrWord* err;
+};
+
+// create-time set-up
+cudaError_t launch_rope_table(float2* tab, int64_t max_pos, int dh, double theta, cudaStream_t st);
+cudaError_t launch_copy_bk(const void* src, int bk_dtype, void* dst, void* dst_t, int mma_dtype, int n_g,
+                           int rk, int cols, cudaStream_t st);
+
+// per-call kernels
+cudaError_t launch_qprep(int mode, const void* q, int q_dtype, const DecodeArgs& a, const int32_t* q_pos,
+                         float qscale, float* qbuf, cudaStream_t st);
+cudaError_t launch_decode_simt(int mode, const DecodeArgs& a, cudaStream_t st);
+cudaError_t launch_combine(const DecodeArgs& a, float* out, float* lse, cudaStream_t st);
+cudaError_t launch_append(void* cache, __half* scale, int cache_dtype, int64_t capacity, int n_g, int rank,
+                          const void* src, int src_dtype, const int32_t* dst_slot, int batch, int n_new,
+                          ErrWord* err, cudaStream_t st);
+cudaError_t launch_debug_dequant(const void* cache, const __half* scale, int cache_dtype, int64_t capacity,
+                                 int n_g, int rank, int batch, int64_t n_tokens, float* out, cudaStream_t st);
+
+// tcgen05 rebuild path (decode_tc.cu); returns cudaErrorNotSupported when the shape has no kernel
+bool tc_supported(const DecodeArgs& a);
+int tc_tile_tokens();
+cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st);
+
+constexpr int kSimtTile = 16;   // tokens per SIMT tile
+
+}  // namespace palu

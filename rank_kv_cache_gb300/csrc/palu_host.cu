@@ -1,0 +1,357 @@
+// C ABI of the G-LRD decode-attention library: validation, workspace layout,
+// launch planning and dispatch. Host code only; kernels live in the other units.
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <new>
+
+#include "palu_attn.h"
+#include "internal.h"
+
+using namespace palu;
+
+namespace {
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int elem_bytes(palu_dtype_t t) { return t == PALU_F32 ? 4 : 2; }
+
+struct WsLayout {
+  size_t err, bk, bkt, rope, qbuf, part_o, part_ml, total;
+  int max_splits;
+  int64_t max_pos;
+};
+
+bool pow2_in(int v, int lo, int hi) { return v >= lo && v <= hi && (v & (v - 1)) == 0; }
+
+palu_status_t check_desc(const palu_attn_desc* d) {
+  if (!d) return PALU_ERR_INVALID_ARG;
+  if (d->abi_version != PALU_ABI_VERSION) return PALU_ERR_INVALID_ARG;
+  if (d->n_heads <= 0 || d->group_size <= 0 || d->n_heads % d->group_size != 0) return PALU_ERR_INVALID_ARG;
+  if (d->max_batch <= 0 || d->max_tokens <= 0 || d->max_position < 0) return PALU_ERR_INVALID_ARG;
+  if (d->max_tokens > (int64_t)1 << 30 || d->max_position > (int64_t)1 << 30) return PALU_ERR_INVALID_ARG;
+  if (d->flags != 0) return PALU_ERR_INVALID_ARG;
+  if (d->mode != PALU_MODE_ROPE && d->mode != PALU_MODE_ABSORBED) return PALU_ERR_INVALID_ARG;
+  if ((unsigned)d->k_dtype > PALU_INT4 || (unsigned)d->v_dtype > PALU_INT4) return PALU_ERR_INVALID_ARG;
+  if ((unsigned)d->bk_dtype > PALU_BF16 || (unsigned)d->q_dtype > PALU_BF16) return PALU_ERR_INVALID_ARG;
+  if (d->mode == PALU_MODE_ROPE && !(d->rope_theta > 0.0 && isfinite(d->rope_theta))) return PALU_ERR_INVALID_ARG;
+  if (d->head_dim <= 0 || d->rank_k <= 0 || d->rank_v <= 0) return PALU_ERR_INVALID_ARG;
+  // shapes and type combinations with a kernel in this build
+  if (d->head_dim != 64 && d->head_dim != 128) return PALU_ERR_UNSUPPORTED;
+  if (!pow2_in(d->group_size, 1, 8)) return PALU_ERR_UNSUPPORTED;
+  if (!pow2_in(d->rank_k, 64, 256) || !pow2_in(d->rank_v, 64, 256)) return PALU_ERR_UNSUPPORTED;
+  if (d->v_dtype != d->k_dtype) return PALU_ERR_UNSUPPORTED;
+  const palu_dtype_t want_bk = d->k_dtype == PALU_INT4 ? PALU_F16 : d->k_dtype;
+  if (d->bk_dtype != want_bk) return PALU_ERR_UNSUPPORTED;
+  return PALU_OK;
+}
+
+WsLayout layout_of(const palu_attn_desc& d) {
+  WsLayout L{};
+  const int64_t n_g = d.n_heads / d.group_size;
+  const int64_t cols = (int64_t)d.group_size * d.head_dim;
+  L.max_pos = d.max_position > 0 ? d.max_position : d.max_tokens;
+  int64_t ms = (d.max_tokens + kSimtTile - 1) / kSimtTile;
+  L.max_splits = int(ms < 1 ? 1 : (ms > 256 ? 256 : ms));
+  size_t off = 0;
+  L.err = off;
+  off = align256(off + 256);
+  L.bk = off;
+  off = align256(off + (size_t)n_g * d.rank_k * cols * elem_bytes(d.bk_dtype));
+  L.bkt = off;
+  if (d.mode == PALU_MODE_ROPE && d.k_dtype != PALU_F32) off = align256(off + (size_t)n_g * cols * d.rank_k * 2);
+  L.rope = off;
+  if (d.mode == PALU_MODE_ROPE) off = align256(off + (size_t)L.max_pos * (d.head_dim / 2) * sizeof(float2));
+  const int qw = d.mode == PALU_MODE_ROPE ? d.head_dim : d.rank_k;
+  L.qbuf = off;
+  off = align256(off + (size_t)d.max_batch * d.n_heads * qw * sizeof(float));
+  L.part_o = off;
+  off = align256(off + (size_t)d.max_batch * d.n_heads * L.max_splits * d.rank_v * sizeof(float));
+  L.part_ml = off;
+  off = align256(off + (size_t)d.max_batch * d.n_heads * L.max_splits * sizeof(float2));
+  L.total = off;
+  return L;
+}
+
+int to_dt(palu_dtype_t t) { return (int)t; }
+
+}  // namespace
+
+struct Trace {
+  bool on = false;
+  int n = 0;                       // recorded pairs
+  int created = 0;                 // events created so far (pairs)
+  cudaEvent_t ev[2 * PALU_TRACE_CAPACITY];
+};
+
+struct palu_attn {
+  palu_attn_desc d;
+  Trace trace;
+  char* ws;
+  size_t ws_bytes;
+  WsLayout L;
+  int n_g;
+  int device;
+  int sm_count;
+  int mma_dtype;
+};
+
+extern "C" {
+
+const char* palu_status_string(palu_status_t s) {
+  switch (s) {
+    case PALU_OK: return "ok";
+    case PALU_ERR_INVALID_ARG: return "invalid argument";
+    case PALU_ERR_UNSUPPORTED: return "unsupported shape or dtype combination";
+    case PALU_ERR_CUDA: return "CUDA runtime error";
+    case PALU_ERR_DEVICE: return "a kernel recorded an out-of-range index";
+    case PALU_ERR_TIMEOUT: return "a bounded device wait gave up";
+    case PALU_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+  }
+  return "unknown status";
+}
+
+palu_status_t palu_attn_workspace_size(const palu_attn_desc* desc, size_t* bytes) {
+  if (!bytes) return PALU_ERR_INVALID_ARG;
+  const palu_status_t st = check_desc(desc);
+  if (st != PALU_OK) return st;
+  *bytes = layout_of(*desc).total;
+  return PALU_OK;
+}
+
+palu_status_t palu_attn_create(const palu_attn_desc* desc, const void* B_k, void* workspace, size_t workspace_bytes,
+                               palu_stream_t stream, palu_attn_t* out) {
+  if (!out) return PALU_ERR_INVALID_ARG;
+  *out = nullptr;
+  palu_status_t st = check_desc(desc);
+  if (st != PALU_OK) return st;
+  if (!B_k) return PALU_ERR_INVALID_ARG;
+  if ((uintptr_t)B_k % 16) return PALU_ERR_INVALID_ARG;
+  const WsLayout L = layout_of(*desc);
+  if (!workspace || (uintptr_t)workspace % 256 || workspace_bytes < L.total) return PALU_ERR_WORKSPACE;
+
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, workspace) != cudaSuccess || attr.type != cudaMemoryTypeDevice) {
+    cudaGetLastError();
+    return PALU_ERR_WORKSPACE;
+  }
+  if (cudaSetDevice(attr.device) != cudaSuccess) return PALU_ERR_CUDA;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, attr.device) != cudaSuccess) return PALU_ERR_CUDA;
+
+  palu_attn* h = new (std::nothrow) palu_attn();
+  if (!h) return PALU_ERR_INVALID_ARG;
+  h->d = *desc;
+  h->ws = static_cast<char*>(workspace);
+  h->ws_bytes = workspace_bytes;
+  h->L = L;
+  h->n_g = desc->n_heads / desc->group_size;
+  h->device = attr.device;
+  h->sm_count = sms;
+  h->mma_dtype = desc->k_dtype == PALU_BF16 ? kBF16 : kF16;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(h->ws + L.err, 0, 256, s);
+  const int cols = desc->group_size * desc->head_dim;
+  void* bkt = (desc->mode == PALU_MODE_ROPE && desc->k_dtype != PALU_F32) ? h->ws + L.bkt : nullptr;
+  if (e == cudaSuccess)
+    e = launch_copy_bk(B_k, to_dt(desc->bk_dtype), h->ws + L.bk, bkt, h->mma_dtype, h->n_g, desc->rank_k, cols, s);
+  if (e == cudaSuccess && desc->mode == PALU_MODE_ROPE)
+    e = launch_rope_table(reinterpret_cast<float2*>(h->ws + L.rope), L.max_pos, desc->head_dim, desc->rope_theta, s);
+  if (e != cudaSuccess) {
+    delete h;
+    return PALU_ERR_CUDA;
+  }
+  *out = h;
+  return PALU_OK;
+}
+
+static void trace_destroy(palu_attn* h) {
+  for (int i = 0; i < 2 * h->trace.created; ++i) cudaEventDestroy(h->trace.ev[i]);
+  h->trace.created = 0;
+  h->trace.n = 0;
+}
+
+palu_status_t palu_destroy(palu_attn_t h) {
+  if (!h) return PALU_OK;
+  if (h->trace.created) {
+    cudaSetDevice(h->device);
+    trace_destroy(h);
+  }
+  delete h;
+  return PALU_OK;
+}
+
+palu_status_t palu_attn_trace_enable(palu_attn_t h, int enable) {
+  if (!h) return PALU_ERR_INVALID_ARG;
+  if (cudaSetDevice(h->device) != cudaSuccess) return PALU_ERR_CUDA;
+  if (!enable) trace_destroy(h);
+  h->trace.on = enable != 0;
+  h->trace.n = 0;
+  return PALU_OK;
+}
+
+palu_status_t palu_attn_trace_read(palu_attn_t h, int* launches, double* total_ms) {
+  if (!h || !launches || !total_ms) return PALU_ERR_INVALID_ARG;
+  if (cudaSetDevice(h->device) != cudaSuccess) return PALU_ERR_CUDA;
+  double sum = 0.0;
+  for (int i = 0; i < h->trace.n; ++i) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(h->trace.ev[2 * i + 1]) != cudaSuccess) return PALU_ERR_CUDA;
+    if (cudaEventElapsedTime(&ms, h->trace.ev[2 * i], h->trace.ev[2 * i + 1]) != cudaSuccess) return PALU_ERR_CUDA;
+    sum += ms;
+  }
+  *launches = h->trace.n;
+  *total_ms = sum;
+  h->trace.n = 0;
+  return PALU_OK;
+}
+
+// Event pair for the next traced launch, or nullptr when tracing is off or the ring is full.
+static cudaEvent_t* trace_slot(palu_attn* h) {
+  Trace& t = h->trace;
+  if (!t.on || t.n >= PALU_TRACE_CAPACITY) return nullptr;
+  if (t.n >= t.created) {
+    if (cudaEventCreate(&t.ev[2 * t.n]) != cudaSuccess) return nullptr;
+    if (cudaEventCreate(&t.ev[2 * t.n + 1]) != cudaSuccess) {
+      cudaEventDestroy(t.ev[2 * t.n]);
+      return nullptr;
+    }
+    t.created = t.n + 1;
+  }
+  return &t.ev[2 * t.n++];
+}
+
+palu_status_t palu_attn_check(palu_attn_t h, palu_stream_t stream) {
+  if (!h) return PALU_ERR_INVALID_ARG;
+  if (cudaSetDevice(h->device) != cudaSuccess) return PALU_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  ErrWord w{};
+  if (cudaMemcpyAsync(&w, h->ws + h->L.err, sizeof(w), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return PALU_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return PALU_ERR_CUDA;
+  if (w.code == 0) return PALU_OK;
+  if (cudaMemsetAsync(h->ws + h->L.err, 0, sizeof(w), s) != cudaSuccess) return PALU_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return PALU_ERR_CUDA;
+  return w.code == kCodeTimeout ? PALU_ERR_TIMEOUT : PALU_ERR_DEVICE;
+}
+
+static palu_status_t check_cache(const palu_attn* h, const palu_cache* c) {
+  if (!c || !c->hk || !c->hv || c->capacity <= 0) return PALU_ERR_INVALID_ARG;
+  if ((uintptr_t)c->hk % 16 || (uintptr_t)c->hv % 16) return PALU_ERR_INVALID_ARG;
+  if (h->d.k_dtype == PALU_INT4 && (!c->k_scale || (uintptr_t)c->k_scale % 2)) return PALU_ERR_INVALID_ARG;
+  if (h->d.v_dtype == PALU_INT4 && (!c->v_scale || (uintptr_t)c->v_scale % 2)) return PALU_ERR_INVALID_ARG;
+  return PALU_OK;
+}
+
+palu_status_t palu_append_latents(palu_attn_t h, const palu_cache* cache, const void* hk_new, const void* hv_new,
+                                  palu_dtype_t src_dtype, const int32_t* dst_slot, int batch, int n_new,
+                                  palu_stream_t stream) {
+  if (!h) return PALU_ERR_INVALID_ARG;
+  palu_status_t st = check_cache(h, cache);
+  if (st != PALU_OK) return st;
+  if (batch < 0 || batch > h->d.max_batch || n_new < 0) return PALU_ERR_INVALID_ARG;
+  if ((unsigned)src_dtype > PALU_BF16) return PALU_ERR_INVALID_ARG;
+  if (batch == 0 || n_new == 0) return PALU_OK;
+  if (!hk_new || !hv_new || !dst_slot) return PALU_ERR_INVALID_ARG;
+  if (cudaSetDevice(h->device) != cudaSuccess) return PALU_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  ErrWord* err = reinterpret_cast<ErrWord*>(h->ws + h->L.err);
+  cudaError_t e = launch_append(cache->hk, static_cast<__half*>(cache->k_scale), to_dt(h->d.k_dtype),
+                                cache->capacity, h->n_g, h->d.rank_k, hk_new, to_dt(src_dtype), dst_slot, batch,
+                                n_new, err, s);
+  if (e == cudaSuccess)
+    e = launch_append(cache->hv, static_cast<__half*>(cache->v_scale), to_dt(h->d.v_dtype), cache->capacity,
+                      h->n_g, h->d.rank_v, hv_new, to_dt(src_dtype), dst_slot, batch, n_new, err, s);
+  return e == cudaSuccess ? PALU_OK : PALU_ERR_CUDA;
+}
+
+palu_status_t palu_decode_attn(palu_attn_t h, const void* q, const palu_cache* cache, const int32_t* seq_lens,
+                               const int32_t* positions, const int32_t* q_pos, int batch, int64_t max_seq_len,
+                               float* out, float* lse, palu_stream_t stream) {
+  if (!h) return PALU_ERR_INVALID_ARG;
+  palu_status_t st = check_cache(h, cache);
+  if (st != PALU_OK) return st;
+  if (batch < 0 || batch > h->d.max_batch) return PALU_ERR_INVALID_ARG;
+  if (batch == 0) return PALU_OK;
+  if (!q || !seq_lens || !out) return PALU_ERR_INVALID_ARG;
+  if ((uintptr_t)out % 16 || (uintptr_t)q % 4) return PALU_ERR_INVALID_ARG;
+  if (max_seq_len < 0 || max_seq_len > h->d.max_tokens || max_seq_len > cache->capacity)
+    return PALU_ERR_INVALID_ARG;
+  if (cudaSetDevice(h->device) != cudaSuccess) return PALU_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  const palu_attn_desc& d = h->d;
+  DecodeArgs a{};
+  a.hk = cache->hk;
+  a.hv = cache->hv;
+  a.k_scale = static_cast<const __half*>(cache->k_scale);
+  a.v_scale = static_cast<const __half*>(cache->v_scale);
+  a.capacity = cache->capacity;
+  a.n_heads = d.n_heads;
+  a.n_g = h->n_g;
+  a.s = d.group_size;
+  a.dh = d.head_dim;
+  a.rk = d.rank_k;
+  a.rv = d.rank_v;
+  a.k_dtype = to_dt(d.k_dtype);
+  a.v_dtype = to_dt(d.v_dtype);
+  a.bk_dtype = to_dt(d.bk_dtype);
+  a.seq_lens = seq_lens;
+  a.positions = (d.mode == PALU_MODE_ROPE) ? positions : nullptr;
+  a.batch = batch;
+  a.max_seq_len = (int)max_seq_len;
+  a.max_pos = h->L.max_pos;
+  a.qbuf = reinterpret_cast<const float*>(h->ws + h->L.qbuf);
+  a.bk = h->ws + h->L.bk;
+  a.bkt = h->ws + h->L.bkt;
+  a.rope = reinterpret_cast<const float2*>(h->ws + h->L.rope);
+  a.part_o = reinterpret_cast<float*>(h->ws + h->L.part_o);
+  a.part_ml = reinterpret_cast<float2*>(h->ws + h->L.part_ml);
+  a.err = reinterpret_cast<ErrWord*>(h->ws + h->L.err);
+
+  const int mode = d.mode == PALU_MODE_ROPE ? kRope : kAbsorbed;
+  const bool use_tc = mode == kRope && tc_supported(a);
+  const int tile = use_tc ? tc_tile_tokens() : kSimtTile;
+  // split-T plan: enough CTAs to cover the SMs about twice
+  const int64_t tiles = max_seq_len > 0 ? (max_seq_len + tile - 1) / tile : 1;
+  const int64_t units = (int64_t)batch * h->n_g;
+  const int64_t target = 2LL * h->sm_count;
+  int64_t splits = (target + units - 1) / units;
+  const int64_t cap = tiles < h->L.max_splits ? tiles : h->L.max_splits;
+  if (splits > cap) splits = cap;
+  if (splits < 1) splits = 1;
+  const int64_t tps = (tiles + splits - 1) / splits;
+  splits = (tiles + tps - 1) / tps;
+  a.n_splits = (int)splits;
+  a.tiles_per_split = (int)tps;
+
+  const float qscale = float(1.4426950408889634 / sqrt((double)d.head_dim));
+  cudaError_t e = launch_qprep(mode, q, to_dt(d.q_dtype), a, q_pos, qscale, const_cast<float*>(a.qbuf), s);
+  cudaEvent_t* tr = (e == cudaSuccess) ? trace_slot(h) : nullptr;
+  if (tr) e = cudaEventRecord(tr[0], s);
+  if (e == cudaSuccess) e = use_tc ? launch_decode_tc(a, s) : launch_decode_simt(mode, a, s);
+  if (tr && e == cudaSuccess) e = cudaEventRecord(tr[1], s);
+  if (e == cudaSuccess) e = launch_combine(a, out, lse, s);
+  return e == cudaSuccess ? PALU_OK : PALU_ERR_CUDA;
+}
+
+palu_status_t palu_debug_dequant(palu_attn_t h, const palu_cache* cache, int which, int batch, int64_t n_tokens,
+                                 float* out, palu_stream_t stream) {
+  if (!h || !out || (which != 0 && which != 1)) return PALU_ERR_INVALID_ARG;
+  palu_status_t st = check_cache(h, cache);
+  if (st != PALU_OK) return st;
+  const palu_dtype_t dt = which == 0 ? h->d.k_dtype : h->d.v_dtype;
+  if (dt != PALU_INT4) return PALU_ERR_INVALID_ARG;
+  if (batch < 0 || batch > h->d.max_batch || n_tokens < 0 || n_tokens > cache->capacity) return PALU_ERR_INVALID_ARG;
+  if (cudaSetDevice(h->device) != cudaSuccess) return PALU_ERR_CUDA;
+  const cudaError_t e = launch_debug_dequant(which == 0 ? cache->hk : cache->hv,
+                                             static_cast<const __half*>(which == 0 ? cache->k_scale : cache->v_scale),
+                                             to_dt(dt), cache->capacity, h->n_g,
+                                             which == 0 ? h->d.rank_k : h->d.rank_v, batch, n_tokens, out,
+                                             reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PALU_OK : PALU_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,280 @@
+// Set-up and small per-call kernels: RoPE table, B_k copies, query preparation,
+// split-T merge, latent append/quantisation and the int4 debug export.
+#include <math.h>
+
+#include "internal.h"
+
+namespace palu {
+
+// ---------------------------------------------------------------------------
+// RoPE table: tab[p][k] = (cos(p w_k), sin(p w_k)), w_k = theta^(-2k/d_h), computed in
+// float64 and rounded to float32 once (rotate-half RoPE with the RoFormer schedule).
+// ---------------------------------------------------------------------------
+__global__ void rope_table_kernel(float2* tab, int64_t max_pos, int half, int dh, double theta) {
+  const int64_t n = max_pos * half;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t p = i / half;
+    const int k = int(i % half);
+    const double w = pow(theta, -2.0 * double(k) / double(dh));
+    double sn, cs;
+    sincos(double(p) * w, &sn, &cs);
+    tab[i] = make_float2(float(cs), float(sn));
+  }
+}
+
+cudaError_t launch_rope_table(float2* tab, int64_t max_pos, int dh, double theta, cudaStream_t st) {
+  const int64_t n = max_pos * (dh / 2);
+  const int blocks = int((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+  rope_table_kernel<<<blocks, 256, 0, st>>>(tab, max_pos, dh / 2, dh, theta);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// B_k copies: dst = B_k as given ([n_g][rk][cols]); dst_t = its per-group transpose
+// [n_g][cols][rk] in the MMA operand type (the K-major B operand of the rebuild GEMM).
+// ---------------------------------------------------------------------------
+__global__ void copy_bk_kernel(const void* src, int bk_dtype, void* dst, void* dst_t, int mma_dtype, int n_g,
+                               int rk, int cols) {
+  const int64_t n = (int64_t)n_g * rk * cols;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int c = int(i % cols);
+    const int m = int((i / cols) % rk);
+    const int g = int(i / ((int64_t)cols * rk));
+    const int esz = bk_dtype == kF32 ? 4 : 2;
+    // plain byte copy of the original layout
+    if (esz == 4) static_cast<float*>(dst)[i] = static_cast<const float*>(src)[i];
+    else static_cast<uint16_t*>(dst)[i] = static_cast<const uint16_t*>(src)[i];
+    if (dst_t) {
+      const float v = load_as_f32(src, bk_dtype, i);
+      const int64_t o = ((int64_t)g * cols + c) * rk + m;
+      if (mma_dtype == kBF16) static_cast<__nv_bfloat16*>(dst_t)[o] = __float2bfloat16_rn(v);
+      else static_cast<__half*>(dst_t)[o] = __float2half_rn(v);
+    }
+  }
+}
+
+cudaError_t launch_copy_bk(const void* src, int bk_dtype, void* dst, void* dst_t, int mma_dtype, int n_g, int rk,
+                           int cols, cudaStream_t st) {
+  const int64_t n = (int64_t)n_g * rk * cols;
+  const int blocks = int((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+  copy_bk_kernel<<<blocks, 256, 0, st>>>(src, bk_dtype, dst, dst_t, mma_dtype, n_g, rk, cols);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Shared helpers for sequence length and positions
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int clamp_seq_len(const DecodeArgs& a, int b) {
+  int T = a.seq_lens[b];
+  const int lim = a.max_seq_len;
+  if (T < 0 || T > lim) {
+    record_error(a.err, kCodeDevice, kErrSeqLen, T, b);
+    T = T < 0 ? 0 : lim;
+  }
+  return T;
+}
+
+// ---------------------------------------------------------------------------
+// Query preparation (one block per (b, head)):
+//   RoPE mode:     q_rot = RoPE(q, q_pos) * qscale                       -> [B][n][dh]
+//   absorbed mode: q'    = (B_k[g][:, j block] q) * qscale  (q B_k^T)    -> [B][n][rk]
+// qscale = log2(e)/sqrt(d_h), so the decode kernels take exp2 of the scores.
+// ---------------------------------------------------------------------------
+__global__ void qprep_rope_kernel(const void* q, int q_dtype, DecodeArgs a, const int32_t* q_pos, float qscale,
+                                  float* qbuf) {
+  const int b = blockIdx.x / a.n_heads;
+  const int i = blockIdx.x % a.n_heads;
+  const int half = a.dh / 2;
+  const int T = clamp_seq_len(a, b);
+  int qp = 0;
+  if (q_pos) qp = q_pos[b];
+  else if (T > 0) qp = a.positions ? a.positions[(int64_t)b * a.capacity + (T - 1)] : (T - 1);
+  if (qp < 0 || qp >= a.max_pos) {
+    if (threadIdx.x == 0) record_error(a.err, kCodeDevice, kErrQueryPos, qp, b);
+    qp = qp < 0 ? 0 : int(a.max_pos - 1);
+  }
+  const int64_t qoff = ((int64_t)b * a.n_heads + i) * a.dh;
+  for (int k = threadIdx.x; k < half; k += blockDim.x) {
+    const float2 cs = a.rope[(int64_t)qp * half + k];
+    const float x0 = load_as_f32(q, q_dtype, qoff + k);
+    const float x1 = load_as_f32(q, q_dtype, qoff + k + half);
+    qbuf[qoff + k] = (x0 * cs.x - x1 * cs.y) * qscale;
+    qbuf[qoff + k + half] = (x1 * cs.x + x0 * cs.y) * qscale;
+  }
+}
+
+__global__ void qprep_absorbed_kernel(const void* q, int q_dtype, DecodeArgs a, float qscale, float* qbuf) {
+  extern __shared__ float qs[];
+  const int b = blockIdx.x / a.n_heads;
+  const int i = blockIdx.x % a.n_heads;
+  const int g = i / a.s, j = i % a.s;
+  const int cols = a.s * a.dh;
+  const int64_t qoff = ((int64_t)b * a.n_heads + i) * a.dh;
+  for (int c = threadIdx.x; c < a.dh; c += blockDim.x) qs[c] = load_as_f32(q, q_dtype, qoff + c);
+  __syncthreads();
+  for (int m = threadIdx.x; m < a.rk; m += blockDim.x) {
+    const int64_t row = ((int64_t)g * a.rk + m) * cols + (int64_t)j * a.dh;
+    float acc = 0.f;
+    for (int c = 0; c < a.dh; ++c) acc = fmaf(load_as_f32(a.bk, a.bk_dtype, row + c), qs[c], acc);
+    qbuf[((int64_t)b * a.n_heads + i) * a.rk + m] = acc * qscale;
+  }
+}
+
+cudaError_t launch_qprep(int mode, const void* q, int q_dtype, const DecodeArgs& a, const int32_t* q_pos,
+                         float qscale, float* qbuf, cudaStream_t st) {
+  const int blocks = a.batch * a.n_heads;
+  if (mode == kRope) qprep_rope_kernel<<<blocks, 64, 0, st>>>(q, q_dtype, a, q_pos, qscale, qbuf);
+  else qprep_absorbed_kernel<<<blocks, 256, a.dh * sizeof(float), st>>>(q, q_dtype, a, qscale, qbuf);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Split-T merge (flash-decoding): with partials (m_k, l_k, o_k) in log2 units,
+//   M = max m_k, L = sum l_k 2^(m_k - M), o = sum o_k 2^(m_k - M) / L, lse = ln2 (M + log2 L).
+// One block per (b, head); empty rows give o = 0, lse = -inf.
+// ---------------------------------------------------------------------------
+__global__ void combine_kernel(DecodeArgs a, float* out, float* lse) {
+  extern __shared__ float wsh[];  // [n_splits] weights
+  const int bh = blockIdx.x;
+  const float2* ml = a.part_ml + (int64_t)bh * a.n_splits;
+  __shared__ float sM, sInvL, sL;
+  if (threadIdx.x < 32) {
+    float M = -INFINITY;
+    for (int k = threadIdx.x; k < a.n_splits; k += 32) M = fmaxf(M, ml[k].x);
+    M = warp_max(M);
+    float L = 0.f;
+    for (int k = threadIdx.x; k < a.n_splits; k += 32) {
+      const float2 v = ml[k];
+      const float w = (v.x == -INFINITY) ? 0.f : exp2f(v.x - M);
+      wsh[k] = w;
+      L += v.y * w;
+    }
+    L = warp_sum(L);
+    if (threadIdx.x == 0) {
+      sM = M;
+      sL = L;
+      sInvL = (L > 0.f) ? 1.f / L : 0.f;
+    }
+  }
+  __syncthreads();
+  const float inv = sInvL;
+  for (int c = threadIdx.x; c < a.rv; c += blockDim.x) {
+    float acc = 0.f;
+    const float* po = a.part_o + (int64_t)bh * a.n_splits * a.rv + c;
+    for (int k = 0; k < a.n_splits; ++k) {
+      const float w = wsh[k];
+      if (w != 0.f) acc = fmaf(po[(int64_t)k * a.rv], w, acc);
+    }
+    out[(int64_t)bh * a.rv + c] = acc * inv;
+  }
+  if (lse && threadIdx.x == 0) lse[bh] = (sL > 0.f) ? (sM + log2f(sL)) * 0.69314718055994531f : -INFINITY;
+}
+
+cudaError_t launch_combine(const DecodeArgs& a, float* out, float* lse, cudaStream_t st) {
+  combine_kernel<<<a.batch * a.n_heads, 256, a.n_splits * sizeof(float), st>>>(a, out, lse);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Append: one warp per (b, new token, group) row.
+// int4 rows: amax over the row in fp32; scale = fp16_rn(min(amax / 7, 65504)) (IEEE division);
+// code = clamp(rint_half_even(h / scale), -7, 7), 0 when the scale is 0; element 2j in the low
+// nibble of byte j, 2j+1 in the high nibble.
+// ---------------------------------------------------------------------------
+__global__ void append_kernel(void* cache, __half* scale, int cache_dtype, int64_t capacity, int n_g, int rank,
+                              const void* src, int src_dtype, const int32_t* dst_slot, int batch, int n_new,
+                              ErrWord* err) {
+  const int warps = blockDim.x / 32;
+  const int64_t row = (int64_t)blockIdx.x * warps + threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  const int64_t rows = (int64_t)batch * n_new * n_g;
+  if (row >= rows) return;
+  const int g = int(row % n_g);
+  const int i = int((row / n_g) % n_new);
+  const int b = int(row / ((int64_t)n_g * n_new));
+  const int dst = dst_slot[b] + i;
+  if (dst < 0 || dst >= capacity) {
+    if (lane == 0) record_error(err, kCodeDevice, kErrSlot, dst, b);
+    return;
+  }
+  const int64_t src_off = row * rank;
+  const int64_t crow = ((int64_t)b * capacity + dst) * n_g + g;
+  if (cache_dtype != kINT4) {
+    for (int e = lane; e < rank; e += 32) {
+      const float v = load_as_f32(src, src_dtype, src_off + e);
+      const int64_t o = crow * rank + e;
+      if (cache_dtype == kF32) static_cast<float*>(cache)[o] = v;
+      else if (cache_dtype == kF16) static_cast<__half*>(cache)[o] = __float2half_rn(v);
+      else static_cast<__nv_bfloat16*>(cache)[o] = __float2bfloat16_rn(v);
+    }
+    return;
+  }
+  // int4: each lane owns `per` consecutive elements (rank / 32 = 2, 4 or 8)
+  const int per = rank / 32;
+  float h[8];
+  float amax = 0.f;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    if (k < per) {
+      h[k] = load_as_f32(src, src_dtype, src_off + lane * per + k);
+      amax = fmaxf(amax, fabsf(h[k]));
+    }
+  }
+  amax = warp_max(amax);
+  const __half sc = __float2half_rn(fminf(__fdiv_rn(amax, 7.0f), 65504.0f));
+  const float sf = __half2float(sc);
+  uint8_t* out = static_cast<uint8_t*>(cache) + crow * (rank / 2) + lane * (per / 2);
+#pragma unroll
+  for (int k = 0; k < 8; k += 2) {
+    if (k < per) {
+      int c0 = 0, c1 = 0;
+      if (sf != 0.f) {
+        c0 = int(fminf(fmaxf(rintf(__fdiv_rn(h[k], sf)), -7.f), 7.f));
+        c1 = int(fminf(fmaxf(rintf(__fdiv_rn(h[k + 1], sf)), -7.f), 7.f));
+      }
+      out[k / 2] = uint8_t((c0 & 0xF) | ((c1 & 0xF) << 4));
+    }
+  }
+  if (lane == 0) scale[crow] = sc;
+}
+
+cudaError_t launch_append(void* cache, __half* scale, int cache_dtype, int64_t capacity, int n_g, int rank,
+                          const void* src, int src_dtype, const int32_t* dst_slot, int batch, int n_new,
+                          ErrWord* err, cudaStream_t st) {
+  const int64_t rows = (int64_t)batch * n_new * n_g;
+  if (rows == 0) return cudaSuccess;
+  const int warps = 8;
+  const int64_t blocks = (rows + warps - 1) / warps;
+  append_kernel<<<(unsigned)blocks, warps * 32, 0, st>>>(cache, scale, cache_dtype, capacity, n_g, rank, src,
+                                                          src_dtype, dst_slot, batch, n_new, err);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Debug export of dequantised int4 latents through the decode kernels' unpack routine.
+// ---------------------------------------------------------------------------
+__global__ void debug_dequant_kernel(const void* cache, const __half* scale, int64_t capacity, int n_g, int rank,
+                                     int batch, int64_t n_tokens, float* out) {
+  const int64_t n = (int64_t)batch * n_tokens * n_g * rank;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int e = int(i % rank);
+    const int64_t r = i / rank;  // (b, t, g) in the output
+    const int g = int(r % n_g);
+    const int64_t t = (r / n_g) % n_tokens;
+    const int64_t b = r / ((int64_t)n_g * n_tokens);
+    const int64_t crow = (b * capacity + t) * n_g + g;
+    out[i] = Latent<Int4>::get(cache, scale, crow, rank, e);
+  }
+}
+
+cudaError_t launch_debug_dequant(const void* cache, const __half* scale, int cache_dtype, int64_t capacity,
+                                 int n_g, int rank, int batch, int64_t n_tokens, float* out, cudaStream_t st) {
+  if (cache_dtype != kINT4) return cudaErrorInvalidValue;
+  const int64_t n = (int64_t)batch * n_tokens * n_g * rank;
+  if (n == 0) return cudaSuccess;
+  const int blocks = int((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+  debug_dequant_kernel<<<blocks, 256, 0, st>>>(cache, scale, capacity, n_g, rank, batch, n_tokens, out);
+  return cudaGetLastError();
+}
+
+}  // namespace palu

@@ -1,0 +1,256 @@
+"""Python binding of the G-LRD decode-attention C ABI (include/palu_attn.h).
+
+Argument marshalling only: every step of the decode path runs in the CUDA
+kernels of ``_lib/libpalu_attn.so``. Importing this package loads that library
+and raises if it has not been built (``rank_kv_cache_gb300.build.build()``);
+there is no CPU fallback.
+
+Low-level functions carry the C names and take raw integers (device pointers,
+stream handles); ``PaluAttention`` and ``LatentCache`` wrap them for torch
+tensors.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libpalu_attn.so")
+
+PALU_ABI_VERSION = 1
+PALU_OK, PALU_ERR_INVALID_ARG, PALU_ERR_UNSUPPORTED, PALU_ERR_CUDA, PALU_ERR_DEVICE, PALU_ERR_TIMEOUT, \
+    PALU_ERR_WORKSPACE = range(7)
+PALU_F32, PALU_F16, PALU_BF16, PALU_INT4 = range(4)
+PALU_MODE_ROPE, PALU_MODE_ABSORBED = 0, 1
+
+DTYPES = {"f32": PALU_F32, "f16": PALU_F16, "bf16": PALU_BF16, "int4": PALU_INT4}
+MODES = {"rope": PALU_MODE_ROPE, "absorbed": PALU_MODE_ABSORBED}
+
+# every symbol include/palu_attn.h declares
+EXPORTS = ("palu_attn_workspace_size", "palu_attn_create", "palu_append_latents", "palu_decode_attn",
+           "palu_destroy", "palu_attn_check", "palu_status_string", "palu_debug_dequant",
+           "palu_attn_trace_enable", "palu_attn_trace_read")
+PALU_TRACE_CAPACITY = 4096
+
+
+class palu_attn_desc(ctypes.Structure):
+    _fields_ = [("abi_version", ctypes.c_int), ("n_heads", ctypes.c_int), ("head_dim", ctypes.c_int),
+                ("group_size", ctypes.c_int), ("rank_k", ctypes.c_int), ("rank_v", ctypes.c_int),
+                ("k_dtype", ctypes.c_int), ("v_dtype", ctypes.c_int), ("bk_dtype", ctypes.c_int),
+                ("q_dtype", ctypes.c_int), ("mode", ctypes.c_int), ("rope_theta", ctypes.c_double),
+                ("max_batch", ctypes.c_int), ("max_tokens", ctypes.c_int64), ("max_position", ctypes.c_int64),
+                ("flags", ctypes.c_uint32)]
+
+
+class palu_cache(ctypes.Structure):
+    _fields_ = [("hk", ctypes.c_void_p), ("hv", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
+                ("v_scale", ctypes.c_void_p), ("capacity", ctypes.c_int64)]
+
+
+class PaluError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {palu_status_string(status)} (status {status})")
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with rank_kv_cache_gb300.build.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, I64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    sig = {
+        "palu_attn_workspace_size": (I, [ctypes.POINTER(palu_attn_desc), ctypes.POINTER(SZ)]),
+        "palu_attn_create": (I, [ctypes.POINTER(palu_attn_desc), P, P, SZ, P, ctypes.POINTER(P)]),
+        "palu_append_latents": (I, [P, ctypes.POINTER(palu_cache), P, P, I, P, I, I, P]),
+        "palu_decode_attn": (I, [P, P, ctypes.POINTER(palu_cache), P, P, P, I, I64, P, P, P]),
+        "palu_destroy": (I, [P]),
+        "palu_attn_check": (I, [P, P]),
+        "palu_status_string": (ctypes.c_char_p, [I]),
+        "palu_debug_dequant": (I, [P, ctypes.POINTER(palu_cache), I, I, I64, P, P]),
+        "palu_attn_trace_enable": (I, [P, I]),
+        "palu_attn_trace_read": (I, [P, ctypes.POINTER(I), ctypes.POINTER(ctypes.c_double)]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype, fn.argtypes = res, args
+    return lib
+
+
+_lib = _load()
+
+
+# ---------------------------------------------------------------------------
+# C-named entry points (raw integers for pointers and streams)
+# ---------------------------------------------------------------------------
+
+def palu_status_string(status: int) -> str:
+    return _lib.palu_status_string(int(status)).decode()
+
+
+def palu_attn_workspace_size(desc: palu_attn_desc):
+    n = ctypes.c_size_t(0)
+    st = _lib.palu_attn_workspace_size(ctypes.byref(desc), ctypes.byref(n))
+    return st, n.value
+
+
+def palu_attn_create(desc: palu_attn_desc, bk_ptr: int, ws_ptr: int, ws_bytes: int, stream: int):
+    h = ctypes.c_void_p()
+    st = _lib.palu_attn_create(ctypes.byref(desc), bk_ptr, ws_ptr, ws_bytes, stream, ctypes.byref(h))
+    return st, h.value
+
+
+def palu_append_latents(h, cache: palu_cache, hk_new: int, hv_new: int, src_dtype: int, dst_slot: int,
+                        batch: int, n_new: int, stream: int) -> int:
+    return _lib.palu_append_latents(h, ctypes.byref(cache), hk_new, hv_new, src_dtype, dst_slot, batch, n_new,
+                                    stream)
+
+
+def palu_decode_attn(h, q: int, cache: palu_cache, seq_lens: int, positions, q_pos, batch: int,
+                     max_seq_len: int, out: int, lse, stream: int) -> int:
+    return _lib.palu_decode_attn(h, q, ctypes.byref(cache), seq_lens, positions, q_pos, batch, max_seq_len, out,
+                                 lse, stream)
+
+
+def palu_destroy(h) -> int:
+    return _lib.palu_destroy(h)
+
+
+def palu_attn_check(h, stream: int) -> int:
+    return _lib.palu_attn_check(h, stream)
+
+
+def palu_debug_dequant(h, cache: palu_cache, which: int, batch: int, n_tokens: int, out: int, stream: int) -> int:
+    return _lib.palu_debug_dequant(h, ctypes.byref(cache), which, batch, n_tokens, out, stream)
+
+
+def palu_attn_trace_enable(h, enable: int) -> int:
+    return _lib.palu_attn_trace_enable(h, int(enable))
+
+
+def palu_attn_trace_read(h):
+    n = ctypes.c_int(0)
+    ms = ctypes.c_double(0.0)
+    st = _lib.palu_attn_trace_read(h, ctypes.byref(n), ctypes.byref(ms))
+    return st, n.value, ms.value
+
+
+def check(status: int, what: str = "palu") -> None:
+    if status != PALU_OK:
+        raise PaluError(status, what)
+
+
+# ---------------------------------------------------------------------------
+# torch helpers
+# ---------------------------------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_handle(stream) -> int:
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else int(t.data_ptr())
+
+
+def _require_contiguous(**tensors):
+    for name, t in tensors.items():
+        if t is not None and not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+
+
+def make_desc(*, n_heads, head_dim, group_size, rank_k, rank_v, latent_dtype, q_dtype, mode, rope_theta=10000.0,
+              max_batch=1, max_tokens=1, max_position=0) -> palu_attn_desc:
+    k = DTYPES[latent_dtype]
+    bk = PALU_F16 if k == PALU_INT4 else k
+    return palu_attn_desc(PALU_ABI_VERSION, n_heads, head_dim, group_size, rank_k, rank_v, k, k, bk,
+                          DTYPES[q_dtype], MODES[mode], float(rope_theta), max_batch, max_tokens, max_position, 0)
+
+
+class LatentCache:
+    """Device latent cache in the layout palu_cache describes ([rows][capacity][n_g][r])."""
+
+    def __init__(self, rows, capacity, n_g, rank_k, rank_v, latent_dtype, device="cuda"):
+        torch = _torch()
+        self.rows, self.capacity, self.n_g = rows, capacity, n_g
+        self.rank_k, self.rank_v, self.latent_dtype = rank_k, rank_v, latent_dtype
+        if latent_dtype == "int4":
+            self.hk = torch.zeros((rows, capacity, n_g, rank_k // 2), dtype=torch.uint8, device=device)
+            self.hv = torch.zeros((rows, capacity, n_g, rank_v // 2), dtype=torch.uint8, device=device)
+            self.k_scale = torch.zeros((rows, capacity, n_g), dtype=torch.float16, device=device)
+            self.v_scale = torch.zeros((rows, capacity, n_g), dtype=torch.float16, device=device)
+        else:
+            dt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[latent_dtype]
+            self.hk = torch.zeros((rows, capacity, n_g, rank_k), dtype=dt, device=device)
+            self.hv = torch.zeros((rows, capacity, n_g, rank_v), dtype=dt, device=device)
+            self.k_scale = self.v_scale = None
+
+    def c_struct(self) -> palu_cache:
+        return palu_cache(_ptr(self.hk), _ptr(self.hv), _ptr(self.k_scale), _ptr(self.v_scale), self.capacity)
+
+
+class PaluAttention:
+    """Owns one handle and its torch-allocated workspace."""
+
+    def __init__(self, bk, *, n_heads, head_dim, group_size, rank_k, rank_v, latent_dtype, q_dtype, mode,
+                 rope_theta=10000.0, max_batch=1, max_tokens=1, max_position=0, stream=None):
+        torch = _torch()
+        self.desc = make_desc(n_heads=n_heads, head_dim=head_dim, group_size=group_size, rank_k=rank_k,
+                              rank_v=rank_v, latent_dtype=latent_dtype, q_dtype=q_dtype, mode=mode,
+                              rope_theta=rope_theta, max_batch=max_batch, max_tokens=max_tokens,
+                              max_position=max_position)
+        st, nbytes = palu_attn_workspace_size(self.desc)
+        check(st, "palu_attn_workspace_size")
+        self.workspace = torch.empty(nbytes + 256, dtype=torch.uint8, device=bk.device)
+        base = int(self.workspace.data_ptr())
+        off = (-base) % 256
+        self.ws_ptr, self.ws_bytes = base + off, nbytes
+        self.n_heads, self.head_dim, self.group_size = n_heads, head_dim, group_size
+        self.rank_k, self.rank_v, self.mode = rank_k, rank_v, mode
+        self._bk = bk.contiguous()
+        st, self.handle = palu_attn_create(self.desc, _ptr(self._bk), self.ws_ptr, self.ws_bytes,
+                                           _stream_handle(stream))
+        check(st, "palu_attn_create")
+
+    def close(self):
+        if getattr(self, "handle", None):
+            palu_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def append(self, cache: LatentCache, hk_new, hv_new, dst_slot, stream=None):
+        torch = _torch()
+        if hk_new.dtype != hv_new.dtype:
+            raise ValueError("hk_new and hv_new must share a dtype")
+        src = {torch.float32: PALU_F32, torch.float16: PALU_F16, torch.bfloat16: PALU_BF16}[hk_new.dtype]
+        _require_contiguous(hk_new=hk_new, hv_new=hv_new, dst_slot=dst_slot)
+        b, n_new = hk_new.shape[0], hk_new.shape[1]
+        st = palu_append_latents(self.handle, cache.c_struct(), _ptr(hk_new), _ptr(hv_new), src, _ptr(dst_slot), b,
+                                 n_new, _stream_handle(stream))
+        check(st, "palu_append_latents")
+
+    def decode(self, q, cache: LatentCache, seq_lens, *, max_seq_len, positions=None, q_pos=None, out=None,
+               lse=None, stream=None):
+        torch = _torch()
+        _require_contiguous(q=q, seq_lens=seq_lens, positions=positions, q_pos=q_pos, out=out, lse=lse)
+        B = q.shape[0]
+        if out is None:
+            out = torch.empty((B, self.n_heads, self.rank_v), dtype=torch.float32, device=q.device)
+        st = palu_decode_attn(self.handle, _ptr(q), cache.c_struct(), _ptr(seq_lens), _ptr(positions),
+                              _ptr(q_pos), B, int(max_seq_len), _ptr(out), _ptr(lse), _stream_handle(stream))
+        check(st, "palu_decode_attn")
+        return out
+
+    def check_device(self, stream=None):
+        check(palu_attn_check(self.handle, _stream_handle(stream)), "palu_attn_check")

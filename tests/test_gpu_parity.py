@@ -1,0 +1,151 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 oracle on the
+same seeded, storage-rounded inputs."""
+import numpy as np
+import pytest
+
+from synthetic import gen
+from tests.gpu_cases import Case, assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu(cuda_device):
+    return cuda_device
+
+
+def test_config1_tiny_fp32_full():
+    c = Case(gen.CONFIGS[1])
+    out, lse = c.run_gpu()
+    ref, lse_ref = c.run_oracle()
+    assert_close(out, ref, lse, lse_ref, f32=True)
+
+
+@pytest.mark.parametrize("T", [1, 2, 127, 128, 129, 1000])
+def test_rope_fp16_tile_edges(T):
+    cfg = gen.CONFIGS[2].with_(T=T, batch=2)
+    c = Case(cfg, seq_lens=[T, max(1, (T * 2) // 3)])
+    out, lse = c.run_gpu()
+    ref, lse_ref = c.run_oracle()
+    assert_close(out, ref, lse, lse_ref)
+
+
+def test_rope_bf16_explicit_positions_query_position_and_empty_row():
+    cfg = gen.CONFIGS[3].with_(T=300, batch=3)
+    rng = np.random.default_rng(5)
+    pos = np.stack([rng.permutation(5000)[:300] for _ in range(3)]).astype(np.int32)
+    c = Case(cfg, seq_lens=[300, 17, 0], positions=pos, q_pos=[4999, 123, 0], max_position=5000)
+    out, lse = c.run_gpu()
+    ref, lse_ref = c.run_oracle()
+    assert np.all(out[2] == 0)
+    assert_close(out, ref, lse, lse_ref)
+
+
+def test_rope_default_query_position_with_positions():
+    cfg = gen.CONFIGS[2].with_(T=200, batch=2)
+    pos = (np.arange(200)[None, :] * 3 + np.array([[7], [1000]])).astype(np.int32)
+    c = Case(cfg, seq_lens=[200, 150], positions=pos, max_position=2000)
+    out, lse = c.run_gpu()
+    ref, lse_ref = c.run_oracle()
+    assert_close(out, ref, lse, lse_ref)
+
+
+def test_absorbed_fp16_ragged():
+    cfg = gen.CONFIGS[4].with_(T=1000, batch=2)
+    c = Case(cfg, seq_lens=[1000, 333])
+    out, lse = c.run_gpu()
+    ref, lse_ref = c.run_oracle()
+    assert_close(out, ref, lse, lse_ref)
+
+
+def test_peaked_softmax_stress():
+    cfg = gen.CONFIGS[2].with_(T=512, batch=1)
+    c = Case(cfg, q_scale=8.0)
+    out, lse = c.run_gpu()
+    ref, lse_ref = c.run_oracle()
+    assert_close(out, ref, lse, lse_ref)
+
+
+def test_split_plan_does_not_change_result():
+    cfg = gen.CONFIGS[2].with_(T=700, batch=1)
+    c = Case(cfg, capacity=4096)
+    a, _ = c.run_gpu()
+    b, _ = c.run_gpu(max_seq_len=4096)
+    ref, _ = c.run_oracle()
+    assert_close(a, ref)
+    assert_close(b, ref)
+
+
+def test_float_append_matches_round_to_nearest():
+    import torch
+    for lat in ("f16", "bf16"):
+        cfg = gen.CONFIGS[2].with_(T=64, batch=2, latent_dtype=lat)
+        c = Case(cfg)
+        want = gen.storage_round(c.inp["hk"], lat)
+        got = c.cache.hk[:, :64].cpu()
+        assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+
+
+def test_int4_append_bit_exact_and_dequant():
+    import torch
+    cfg = gen.CONFIGS[5].with_(T=300, batch=2)
+    c = Case(cfg)
+    pk, sk, pv, sv = c.ref_packed
+    np.testing.assert_array_equal(c.cache.hk[:, :300].cpu().numpy(), pk)
+    np.testing.assert_array_equal(c.cache.hv[:, :300].cpu().numpy(), pv)
+    np.testing.assert_array_equal(c.cache.k_scale[:, :300].cpu().numpy().view(np.uint16), sk.view(np.uint16))
+    np.testing.assert_array_equal(c.cache.v_scale[:, :300].cpu().numpy().view(np.uint16), sv.view(np.uint16))
+    from rank_kv_cache_gb300 import palu as P
+    for which, ref in ((0, c.hk64), (1, c.hv64)):
+        out = torch.empty((2, 300, cfg.n_groups, cfg.rank), dtype=torch.float32, device=c.dev)
+        st = P.palu_debug_dequant(c.attn.handle, c.cache.c_struct(), which, 2, 300, out.data_ptr(),
+                                  int(torch.cuda.current_stream().cuda_stream))
+        assert st == 0
+        np.testing.assert_array_equal(out.cpu().numpy(), ref)
+
+
+def test_int4_rope_hadamard_ragged():
+    cfg = gen.CONFIGS[5].with_(T=700, batch=2)
+    c = Case(cfg, seq_lens=[700, 259])
+    out, lse = c.run_gpu()
+    ref, lse_ref = c.run_oracle()
+    assert_close(out, ref, lse, lse_ref)
+
+
+def test_device_error_word_on_bad_position():
+    from rank_kv_cache_gb300 import palu as P
+    cfg = gen.CONFIGS[2].with_(T=64, batch=1)
+    pos = np.arange(64, dtype=np.int32)[None, :].copy()
+    pos[0, 10] = 100000  # outside the 64-entry table
+    c = Case(cfg, positions=pos)
+    with pytest.raises(P.PaluError) as ei:
+        c.run_gpu()
+    assert ei.value.status == P.PALU_ERR_DEVICE
+    c.attn.check_device()  # cleared
+
+
+# --- full workload sizes: every head where the oracle is quick, else sampled heads ---
+
+def _sample_heads(B, n, k=6, seed=0):
+    rng = np.random.default_rng(seed)
+    hs = {(0, 0), (B - 1, n - 1)}
+    while len(hs) < k:
+        hs.add((int(rng.integers(B)), int(rng.integers(n))))
+    return sorted(hs)
+
+
+def test_full_config2_all_heads():
+    c = Case(gen.CONFIGS[2])
+    out, lse = c.run_gpu()
+    ref, lse_ref = c.run_oracle()
+    assert_close(out, ref, lse, lse_ref)
+
+
+@pytest.mark.parametrize("cid,T", [(3, 16384), (3, 32768), (4, 65536), (5, 65536)])
+def test_full_size_sampled_heads(cid, T):
+    cfg = gen.CONFIGS[cid].with_(T=T)
+    c = Case(cfg)
+    out, lse = c.run_gpu()
+    heads = _sample_heads(cfg.batch, cfg.n_heads)
+    ref, lse_ref = c.run_oracle(heads=heads)
+    assert_close(out, ref, lse, lse_ref, heads=heads)
