@@ -174,6 +174,32 @@ palu_status_t palu_decode_attn(palu_attn_t h, const void* q, const palu_cache* c
                                int batch, int64_t max_seq_len, float* out, float* lse,
                                palu_stream_t stream);
 
+/*
+ * Absorbed-mode decode for callers that cannot allocate device memory (a plugin
+ * whose host owns every allocation, an engine with a fixed memory plan, code that
+ * must not allocate once serving starts). The pages have no counterpart to it.
+ * It takes no handle and no workspace: B_k (device, [n_g][rank_k][s * head_dim]
+ * in desc->bk_dtype) and the query are read directly, and the scratch (error
+ * word, absorbed queries, split partials) lives in one fixed 8 MiB device array
+ * inside this library, which every GPU that loads the library holds until the
+ * process exits. It calls no cudaMalloc, cudaFree or other allocating routine.
+ *   - desc->mode must be PALU_MODE_ABSORBED (else PALU_ERR_UNSUPPORTED);
+ *     arguments as for palu_decode_attn, without positions and q_pos.
+ *   - A request whose scratch (4 bytes x batch x n_heads x (rank_k + rank_v) for
+ *     one split, plus alignment) does not fit in 8 MiB returns PALU_ERR_WORKSPACE
+ *     before anything is queued; larger T only lowers the split count.
+ *   - The first call on a device looks up the array's address on that device
+ *     (cudaGetSymbolAddress), so make that first call before any stream capture.
+ *   - Every call shares the one array, and its contents persist between calls;
+ *     the error word is cleared at the start of each call. Calls that overlap on
+ *     the GPU (different streams, or host threads racing) race on the scratch:
+ *     serialise them. Out-of-range sequence lengths are clamped; there is no
+ *     handle through which to report them.
+ */
+palu_status_t palu_decode_attn_noalloc(const palu_attn_desc* desc, const void* B_k, const void* q,
+                                       const palu_cache* cache, const int32_t* seq_lens, int batch,
+                                       int64_t max_seq_len, float* out, float* lse, palu_stream_t stream);
+
 /* Free the host handle. Does not synchronise: no work on it may be in flight. NULL is fine. */
 palu_status_t palu_destroy(palu_attn_t h);
 

@@ -29,7 +29,7 @@ MODES = {"rope": PALU_MODE_ROPE, "absorbed": PALU_MODE_ABSORBED}
 # every symbol include/palu_attn.h declares
 EXPORTS = ("palu_attn_workspace_size", "palu_attn_create", "palu_append_latents", "palu_decode_attn",
            "palu_destroy", "palu_attn_check", "palu_status_string", "palu_debug_dequant",
-           "palu_attn_trace_enable", "palu_attn_trace_read")
+           "palu_attn_trace_enable", "palu_attn_trace_read", "palu_decode_attn_noalloc")
 PALU_TRACE_CAPACITY = 4096
 
 
@@ -69,6 +69,8 @@ def _load():
         "palu_debug_dequant": (I, [P, ctypes.POINTER(palu_cache), I, I, I64, P, P]),
         "palu_attn_trace_enable": (I, [P, I]),
         "palu_attn_trace_read": (I, [P, ctypes.POINTER(I), ctypes.POINTER(ctypes.c_double)]),
+        "palu_decode_attn_noalloc": (I, [ctypes.POINTER(palu_attn_desc), P, P, ctypes.POINTER(palu_cache), P, I,
+                                         I64, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -132,6 +134,13 @@ def palu_attn_trace_read(h):
     ms = ctypes.c_double(0.0)
     st = _lib.palu_attn_trace_read(h, ctypes.byref(n), ctypes.byref(ms))
     return st, n.value, ms.value
+
+
+def palu_decode_attn_noalloc(desc: palu_attn_desc, bk: int, q: int, cache: palu_cache, seq_lens: int, batch: int,
+                             max_seq_len: int, out: int, lse, stream: int) -> int:
+    """Absorbed-mode decode with the library's fixed device scratch (no allocation anywhere)."""
+    return _lib.palu_decode_attn_noalloc(ctypes.byref(desc), bk, q, ctypes.byref(cache), seq_lens, batch,
+                                         max_seq_len, out, lse, stream)
 
 
 def check(status: int, what: str = "palu") -> None:
