@@ -421,12 +421,18 @@ def main(argv=None):
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--batch", type=int, default=None, help="override the workload's batch (profiling runs)")
+    ap.add_argument("--tokens", type=int, default=None, help="override the workload's T (profiling runs)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     from synthetic import gen
     cid, T = WORKLOADS[args.workload]
     cfg = gen.CONFIGS[cid] if T is None else gen.CONFIGS[cid].with_(T=T)
+    if args.batch is not None:
+        cfg = cfg.with_(batch=args.batch)
+    if args.tokens is not None:
+        cfg = cfg.with_(T=args.tokens)
     res = run_reference(args, cfg, args.workload) if args.impl == "reference" else run_gpu(args, cfg, args.workload)
     if res is not None:
         print(json.dumps(res), flush=True)

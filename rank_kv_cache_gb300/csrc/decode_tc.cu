@@ -1,10 +1,599 @@
-// tcgen05 rebuild path for the RoPE mode (placeholder until the kernel lands).
+// RoPE-mode decode attention with the key rebuild on tcgen05 tensor cores.
+//
+// "Palu: KV-Cache Compression With Low-Rank Projection", supplementary section
+// (online-rebuild score kernel): the latent keys H (L x r) are streamed tile by
+// tile, each tile is multiplied by the reconstruction matrix B on chip, RoPE is
+// applied to the rebuilt keys and they are dotted with the query; intermediates
+// never leave the chip. Here, per CTA:
+//   * one (batch row b, group g, head pair hp, T-split) unit; the head pair's
+//     slice of B_k^T (256 rows x r, K-major) stays in shared memory;
+//   * warp 0 streams 128-token x 64-rank chunks of H_k,g by TMA (128-byte swizzle)
+//     through a 3-stage ring; warp 10 streams 16-token chunks of H_v,g by TMA
+//     through a 5-slot ring;
+//   * warp 1 issues tcgen05.mma (M=128 tokens, N=256 = 2 heads x d_h, K=r) into
+//     one of two TMEM accumulators;
+//   * the score warpgroup (warps 2-5, one token row per thread, read with
+//     tcgen05.ld) rotates every rebuilt key pair at the token's position and dots
+//     it with the rotated query, writing the tile's scores to a double-buffered
+//     slot in shared memory;
+//   * the softmax warpgroup (warps 6-9) runs the online softmax (base 2) on the
+//     previous tile's scores and accumulates p H_v in latent space on CUDA cores,
+//     so scoring and p H_v of consecutive tiles overlap; the T-split partials go
+//     to the merge kernel.
+// RoPE angles: pair k's frequency is held as a 64-bit fixed-point fraction of a
+// turn F_k, so position p's phase is (p * F_k mod 2^64) / 2^64 turns: integer
+// range reduction with no rounding (phase accumulation as in direct digital
+// synthesis); the top 32 bits become an angle in [-pi, pi) for __sincosf.
+// Every mbarrier wait is bounded; a time-out sets the workspace error word
+// (PALU_ERR_TIMEOUT), all roles stop, in-flight copies are drained and TMEM freed.
+#include <cuda.h>
+
+#include <mutex>
+
 #include "internal.h"
+#include "tc_ptx.cuh"
 
 namespace palu {
 
-bool tc_supported(const DecodeArgs&) { return false; }
-int tc_tile_tokens() { return 128; }
-cudaError_t launch_decode_tc(const DecodeArgs&, cudaStream_t) { return cudaErrorNotSupported; }
+namespace {
+
+constexpr int kTile = 128;                       // tokens per tile (MMA M)
+constexpr int kHeads = 2;                        // heads per CTA
+constexpr int kDh = 128;                         // head dim
+constexpr int kHalf = kDh / 2;                   // RoPE pairs per head
+constexpr int kN = kHeads * kDh;                 // MMA N
+constexpr int kRank = 256;                       // r_k = r_v (MMA K)
+constexpr int kKChunk = 64;                      // K elements per 128-byte swizzled row
+constexpr int kChunks = kRank / kKChunk;         // 4
+constexpr int kStages = 3;                       // H_k ring
+constexpr int kAStage = kTile * kKChunk * 2;     // 16 KB
+constexpr int kBChunk = kN * kKChunk * 2;        // 32 KB
+constexpr int kBBytes = kBChunk * kChunks;       // 128 KB
+constexpr int kVTok = 16;                        // tokens per H_v chunk
+constexpr int kVChunks = kTile / kVTok;          // 8 per tile
+constexpr int kVSlots = 5;                       // H_v ring
+constexpr int kVSlot = kVTok * kRank * 2;        // 8 KB
+constexpr int kWgThreads = 128;                  // one warpgroup
+// warps: 0 H_k/B producer, 1 MMA issuer, 2-5 score warpgroup, 6-9 softmax/PV warpgroup, 10 H_v producer
+constexpr int kThreads = 11 * 32;
+constexpr int kBarScore = 1;                     // named barrier of the score warpgroup
+constexpr int kBarPv = 2;                        // named barrier of the softmax/PV warpgroup
+constexpr uint32_t kTmemCols = 512;              // two N=256 fp32 accumulators
+constexpr uint64_t kWaitNs = 1000000000ull;      // 1 s per wait
+constexpr float kTurnToRad = 1.4629180792671596e-09f;  // 2 pi / 2^32
+
+// shared-memory map (offsets from a 1024-byte aligned base)
+constexpr int kOffB = 0;
+constexpr int kOffA = kOffB + kBBytes;
+constexpr int kOffV = kOffA + kStages * kAStage;
+constexpr int kOffBar = kOffV + kVSlots * kVSlot;
+// barriers: fullA[3], emptyA[3], bfull[4], tfull[2], tempty[2], vfull[5], vempty[5], sready[2], sfree[2], mma_done
+constexpr int kNumBars = 2 * kStages + kChunks + 2 + 2 + 2 * kVSlots + 2 + 2 + 1;
+constexpr int kOffMisc = kOffBar + 8 * kNumBars;
+constexpr int kOffQ = (kOffMisc + 16 + 15) & ~15;           // float4 [kHalf]: (qa0, qa1, qb0, qb1)
+constexpr int kOffF = kOffQ + kHalf * 16;                   // uint64 [kHalf]
+constexpr int kOffS = kOffF + kHalf * 8;                    // float2 [2][kTile] scores
+constexpr int kOffRed = kOffS + 2 * kTile * 8;              // float2 [4]
+constexpr int kOffP = kOffRed + 4 * 8;                      // float2 [kTile]
+constexpr int kOffL = kOffP + kTile * 8;                    // float2 [4]
+constexpr int kSmemBytes = kOffL + 4 * 8;
+constexpr int kSmemAlloc = kSmemBytes + 1024;
+constexpr int kOffO = kOffV;                                // float [4][kHeads][kRank], reuses the H_v ring
+static_assert(4 * kHeads * kRank * 4 <= kVSlots * kVSlot, "output reduction fits the H_v ring");
+static_assert(kSmemAlloc <= 232448, "shared memory budget");
+
+struct TcParams {
+  DecodeArgs a;
+  int hp_count;   // head pairs per group
+  int bf16;       // MMA operand type
+};
+
+template <typename VT>
+__device__ __forceinline__ void unpack8(const uint4& u, float* h);
+template <>
+__device__ __forceinline__ void unpack8<__half>(const uint4& u, float* h) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+    h[2 * i] = f.x;
+    h[2 * i + 1] = f.y;
+  }
+}
+template <>
+__device__ __forceinline__ void unpack8<__nv_bfloat16>(const uint4& u, float* h) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    h[2 * i] = __uint_as_float(w[i] << 16);
+    h[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+__device__ __forceinline__ int token_position(const DecodeArgs& a, int b, int t, bool valid) {
+  int pos = t;
+  if (valid && a.positions) pos = a.positions[(int64_t)b * a.capacity + t];
+  if (pos < 0 || pos >= a.max_pos) {
+    if (valid) record_error(a.err, kCodeDevice, kErrPosition, pos, b);
+    pos = pos < 0 ? 0 : int(a.max_pos - 1);
+  }
+  return pos;
+}
+
+template <typename VT>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tm_hk, const __grid_constant__ CUtensorMap tm_hv,
+                     const __grid_constant__ CUtensorMap tm_b, const TcParams P) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const DecodeArgs& a = P.a;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int hp = blockIdx.x % P.hp_count, split = blockIdx.x / P.hp_count;
+  const int g = blockIdx.y, b = blockIdx.z;
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* fullA = bars;
+  uint64_t* emptyA = fullA + kStages;
+  uint64_t* bfull = emptyA + kStages;
+  uint64_t* tfull = bfull + kChunks;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* vfull = tempty + 2;
+  uint64_t* vempty = vfull + kVSlots;
+  uint64_t* sready = vempty + kVSlots;
+  uint64_t* sfree = sready + 2;
+  uint64_t* mma_done = sfree + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+  float4* qs = reinterpret_cast<float4*>(smem + kOffQ);
+  uint64_t* Fs = reinterpret_cast<uint64_t*>(smem + kOffF);
+  float2* sbuf = reinterpret_cast<float2*>(smem + kOffS);
+  float2* red = reinterpret_cast<float2*>(smem + kOffRed);
+  float2* pbuf = reinterpret_cast<float2*>(smem + kOffP);
+  float* ored = reinterpret_cast<float*>(smem + kOffO);
+  float2* lred = reinterpret_cast<float2*>(smem + kOffL);
+
+  // this CTA's token range
+  int T = a.seq_lens[b];
+  if (T < 0 || T > a.max_seq_len) {
+    if (threadIdx.x == 0 && split == 0 && hp == 0 && g == 0) record_error(a.err, kCodeDevice, kErrSeqLen, T, b);
+    T = T < 0 ? 0 : a.max_seq_len;
+  }
+  const int span = a.tiles_per_split * kTile;
+  const int t_begin = split * span;
+  const int t_end = min(T, t_begin + span);
+  const int n_tiles = t_end > t_begin ? (t_end - t_begin + kTile - 1) / kTile : 0;
+  const int head0 = g * a.s + hp * kHeads;  // first head of this CTA within the row
+  const int row0 = b * (int)a.capacity;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      tc::mbar_init(&fullA[i], 1);
+      tc::mbar_init(&emptyA[i], 1);
+    }
+    for (int i = 0; i < kChunks; ++i) tc::mbar_init(&bfull[i], 1);
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&tfull[i], 1);
+      tc::mbar_init(&tempty[i], 4);
+      tc::mbar_init(&sready[i], 4);
+      tc::mbar_init(&sfree[i], 4);
+    }
+    for (int i = 0; i < kVSlots; ++i) {
+      tc::mbar_init(&vfull[i], 1);
+      tc::mbar_init(&vempty[i], 4);
+    }
+    tc::mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_slot, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  if (warp >= 2 && warp < 6) {
+    // rotate the two heads' queries at q_pos (RoPE table, float64-derived), scale by
+    // log2(e)/sqrt(d_h), and keep them as (q_a, q_b) pairs per rotation pair
+    const int i = threadIdx.x - 64;
+    const int j = i / kHalf, k = i % kHalf;
+    int qp = 0;
+    if (a.q_pos) qp = a.q_pos[b];
+    else if (T > 0) qp = a.positions ? a.positions[(int64_t)b * a.capacity + (T - 1)] : (T - 1);
+    if (qp < 0 || qp >= a.max_pos) {
+      if (i == 0 && split == 0 && hp == 0 && g == 0) record_error(a.err, kCodeDevice, kErrQueryPos, qp, b);
+      qp = qp < 0 ? 0 : int(a.max_pos - 1);
+    }
+    const float2 cs = a.rope[(int64_t)qp * kHalf + k];
+    const int64_t qoff = ((int64_t)b * a.n_heads + head0 + j) * kDh;
+    const float x0 = load_as_f32(a.q, a.q_dtype, qoff + k);
+    const float x1 = load_as_f32(a.q, a.q_dtype, qoff + k + kHalf);
+    float* qf = reinterpret_cast<float*>(&qs[k]);
+    qf[j] = (x0 * cs.x - x1 * cs.y) * a.qscale;
+    qf[2 + j] = (x1 * cs.x + x0 * cs.y) * a.qscale;
+    if (j == 0) Fs[k] = a.phase[k];
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ H_k / B producer
+    if (lane == 0 && n_tiles > 0) {
+      tc::tma_prefetch(&tm_hk);
+      tc::tma_prefetch(&tm_b);
+      const int brow = g * (a.s * kDh) + hp * kN;
+      for (int kc = 0; kc < kChunks; ++kc) {
+        tc::mbar_arrive_expect_tx(&bfull[kc], kBChunk);
+        tc::tma_load_2d(smem + kOffB + kc * kBChunk, &tm_b, &bfull[kc], kc * kKChunk, brow);
+      }
+      int stage = 0, issued = 0;
+      uint32_t round = 0;
+      bool ok = true;
+      for (int it = 0; it < n_tiles && ok; ++it) {
+        const int t0 = t_begin + it * kTile;
+        for (int kc = 0; kc < kChunks; ++kc) {
+          if (!tc::mbar_wait_bounded(&emptyA[stage], (round & 1) ^ 1, abort_flag, kWaitNs)) {
+            ok = false;
+            break;
+          }
+          tc::mbar_arrive_expect_tx(&fullA[stage], kAStage);
+          tc::tma_load_3d(smem + kOffA + stage * kAStage, &tm_hk, &fullA[stage], kc * kKChunk, g, row0 + t0);
+          ++issued;
+          if (++stage == kStages) {
+            stage = 0;
+            ++round;
+          }
+        }
+      }
+      if (!ok) {
+        // drain the copies still in flight before the CTA may exit
+        volatile int quiet = 0;
+        for (int k = 0, s = stage, r = (int)round; k < (issued < kStages ? issued : kStages); ++k) {
+          if (--s < 0) {
+            s = kStages - 1;
+            --r;
+          }
+          tc::mbar_wait_bounded(&fullA[s], uint32_t(r) & 1, &quiet, kWaitNs / 10);
+        }
+        for (int kc = 0; kc < kChunks; ++kc) tc::mbar_wait_bounded(&bfull[kc], 0, &quiet, kWaitNs / 10);
+      }
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ H_v producer
+    if (lane == 0 && n_tiles > 0) {
+      tc::tma_prefetch(&tm_hv);
+      int issued = 0;
+      bool ok = true;
+      for (int it = 0; it < n_tiles && ok; ++it) {
+        const int t0 = t_begin + it * kTile;
+        for (int ch = 0; ch < kVChunks; ++ch) {
+          const int vi = it * kVChunks + ch;
+          const int slot = vi % kVSlots;
+          if (!tc::mbar_wait_bounded(&vempty[slot], ((vi / kVSlots) & 1) ^ 1, abort_flag, kWaitNs)) {
+            ok = false;
+            break;
+          }
+          tc::mbar_arrive_expect_tx(&vfull[slot], kVSlot);
+          tc::tma_load_3d(smem + kOffV + slot * kVSlot, &tm_hv, &vfull[slot], 0, g, row0 + t0 + ch * kVTok);
+          ++issued;
+        }
+      }
+      if (!ok) {
+        volatile int quiet = 0;
+        for (int vi = (issued > kVSlots ? issued - kVSlots : 0); vi < issued; ++vi)
+          tc::mbar_wait_bounded(&vfull[vi % kVSlots], (vi / kVSlots) & 1, &quiet, kWaitNs / 10);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n_tiles > 0) {
+      const uint32_t idesc = tc::idesc_f16(kTile, kN, P.bf16 != 0);
+      bool ok = true;
+      int stage = 0;
+      uint32_t round = 0;
+      const uint32_t a_base = tc::smem_addr(smem + kOffA);
+      const uint32_t b_base = tc::smem_addr(smem + kOffB);
+      for (int it = 0; it < n_tiles && ok; ++it) {
+        const int buf = it & 1;
+        const uint32_t use = it >> 1;
+        if (!tc::mbar_wait_bounded(&tempty[buf], (use & 1) ^ 1, abort_flag, kWaitNs)) {
+          ok = false;
+          break;
+        }
+        tc::tc_fence_after();
+        const uint32_t d = tmem_base + buf * kN;
+        for (int kc = 0; kc < kChunks; ++kc) {
+          if (it == 0 && !tc::mbar_wait_bounded(&bfull[kc], 0, abort_flag, kWaitNs)) {
+            ok = false;
+            break;
+          }
+          if (!tc::mbar_wait_bounded(&fullA[stage], round & 1, abort_flag, kWaitNs)) {
+            ok = false;
+            break;
+          }
+          tc::tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < kKChunk / 16; ++k) {
+            const uint64_t ad = tc::sdesc_k_sw128(a_base + stage * kAStage + k * 32);
+            const uint64_t bd = tc::sdesc_k_sw128(b_base + kc * kBChunk + k * 32);
+            tc::umma_f16(d, ad, bd, idesc, (kc | k) != 0);
+          }
+          tc::umma_commit(&emptyA[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            ++round;
+          }
+        }
+        if (!ok) break;
+        tc::umma_commit(&tfull[buf]);
+      }
+      // every MMA this thread issued has completed once mma_done flips
+      tc::umma_commit(mma_done);
+      volatile int quiet = 0;
+      tc::mbar_wait_bounded(mma_done, 0, &quiet, kWaitNs);
+    }
+  } else if (warp < 6) {
+    // ------------------------------------------------------------ score warpgroup
+    // thread = one token row of the tile: RoPE-rotate each rebuilt key pair at the
+    // token's position and dot it with the rotated query, for both heads.
+    const int quad = warp & 3;               // TMEM lane quadrant this warp may access
+    const int row = quad * 32 + lane;
+    int pos_next = token_position(a, b, t_begin + row, t_begin + row < t_end);
+    for (int it = 0; it < n_tiles; ++it) {
+      const int buf = it & 1;
+      const uint32_t use = it >> 1;
+      const int t0 = t_begin + it * kTile;
+      const bool valid = t0 + row < t_end;
+      const uint32_t upos = uint32_t(pos_next);
+      if (it + 1 < n_tiles) pos_next = token_position(a, b, t0 + kTile + row, t0 + kTile + row < t_end);
+
+      const bool got = tc::mbar_wait_bounded(&tfull[buf], use & 1, abort_flag, kWaitNs) &&
+                       tc::mbar_wait_bounded(&sfree[buf], (use & 1) ^ 1, abort_flag, kWaitNs);
+      if (tc::named_bar_or(kBarScore, kWgThreads, !got)) break;  // one decision for the warpgroup
+      tc::tc_fence_after();
+
+      float s0a = 0.f, s0b = 0.f, s1a = 0.f, s1b = 0.f;
+      const uint32_t tbase = tmem_base + (uint32_t(quad * 32) << 16) + buf * kN;
+#pragma unroll 1
+      for (int a0 = 0; a0 < kHalf; a0 += 16) {
+        // issue the four TMEM loads of this chunk (pairs a0..a0+15 of both heads), compute
+        // the chunk's cos/sin while they are in flight, then wait
+        uint32_t k0[32], k1[32];
+        tc::tmem_ld16x2_nowait(tbase + a0, tbase + kHalf + a0, k0);
+        tc::tmem_ld16x2_nowait(tbase + kDh + a0, tbase + kDh + kHalf + a0, k1);
+        float cs[16], sn[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const uint64_t F = Fs[a0 + u];
+          const uint32_t top = __umulhi(upos, uint32_t(F)) + upos * uint32_t(F >> 32);
+          __sincosf(float(int32_t(top)) * kTurnToRad, &sn[u], &cs[u]);
+        }
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const float4 q4 = qs[a0 + u];     // (qa0, qa1, qb0, qb1)
+          const float ka0 = __uint_as_float(k0[u]), kb0 = __uint_as_float(k0[16 + u]);
+          const float ka1 = __uint_as_float(k1[u]), kb1 = __uint_as_float(k1[16 + u]);
+          const float t0 = fmaf(q4.x, ka0, q4.z * kb0), v0 = fmaf(q4.z, ka0, -q4.x * kb0);
+          const float t1 = fmaf(q4.y, ka1, q4.w * kb1), v1 = fmaf(q4.w, ka1, -q4.y * kb1);
+          if (u & 1) {
+            s0b = fmaf(sn[u], v0, fmaf(cs[u], t0, s0b));
+            s1b = fmaf(sn[u], v1, fmaf(cs[u], t1, s1b));
+          } else {
+            s0a = fmaf(sn[u], v0, fmaf(cs[u], t0, s0a));
+            s1a = fmaf(sn[u], v1, fmaf(cs[u], t1, s1a));
+          }
+        }
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&tempty[buf]);
+      sbuf[buf * kTile + row] = valid ? make_float2(s0a + s0b, s1a + s1b) : make_float2(-INFINITY, -INFINITY);
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&sready[buf]);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax / PV warpgroup
+    const int e = warp - 6;                  // 0..3
+    const int ei = threadIdx.x - 6 * 32;     // 0..127: token row for the softmax
+    float m_run0 = -INFINITY, m_run1 = -INFINITY;
+    float l0 = 0.f, l1 = 0.f;
+    float acc0[8], acc1[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) acc0[c] = acc1[c] = 0.f;
+    bool aborted = false;  // warpgroup-uniform: only ever set from a barrier-OR
+    bool broken = false;   // this warp's own H_v wait gave up
+
+    for (int it = 0; it < n_tiles; ++it) {
+      const int buf = it & 1;
+      const uint32_t use = it >> 1;
+      const int t0 = t_begin + it * kTile;
+      const bool got = tc::mbar_wait_bounded(&sready[buf], use & 1, abort_flag, kWaitNs);
+      if (tc::named_bar_or(kBarPv, kWgThreads, !got || broken)) {
+        aborted = true;
+        break;
+      }
+      const float2 sc = sbuf[buf * kTile + ei];
+      __syncwarp();
+      if ((ei & 31) == 0) tc::mbar_arrive(&sfree[buf]);
+
+      // online softmax over the tile (uniform running max across the 128 threads)
+      const float w0 = warp_max(sc.x), w1 = warp_max(sc.y);
+      if (lane == 0) red[e] = make_float2(w0, w1);
+      tc::named_bar(kBarPv, kWgThreads);
+      float tm0 = -INFINITY, tm1 = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        tm0 = fmaxf(tm0, red[k].x);
+        tm1 = fmaxf(tm1, red[k].y);
+      }
+      const float mn0 = fmaxf(m_run0, tm0), mn1 = fmaxf(m_run1, tm1);
+      const float al0 = (mn0 == -INFINITY) ? 1.f : exp2f(m_run0 - mn0);
+      const float al1 = (mn1 == -INFINITY) ? 1.f : exp2f(m_run1 - mn1);
+      const float p0 = (sc.x == -INFINITY) ? 0.f : exp2f(sc.x - mn0);
+      const float p1 = (sc.y == -INFINITY) ? 0.f : exp2f(sc.y - mn1);
+      m_run0 = mn0;
+      m_run1 = mn1;
+      l0 = l0 * al0 + p0;
+      l1 = l1 * al1 + p1;
+      pbuf[ei] = make_float2(p0, p1);
+      tc::named_bar(kBarPv, kWgThreads);
+
+      // p H_v from the staged 16-token chunks; warp e takes 4 tokens of each chunk and
+      // lane owns columns 8*lane..8*lane+7
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        acc0[c] *= al0;
+        acc1[c] *= al1;
+      }
+      // Waits here are bounded but not followed by a warpgroup barrier: a warp whose wait
+      // gave up skips the arithmetic and the tile-level decision above ends the loop for all.
+      for (int ch = 0; ch < kVChunks; ch += 2) {
+        uint4 u[8];
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          const int vi = it * kVChunks + ch + c2;
+          const int slot = vi % kVSlots;
+          const bool vgot = tc::mbar_wait_bounded(&vfull[slot], (vi / kVSlots) & 1, abort_flag, kWaitNs);
+          if (!vgot) broken = true;
+          const uint8_t* vs = smem + kOffV + slot * kVSlot + (e * 4) * (kRank * 2) + lane * 16;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) u[c2 * 4 + k] = *reinterpret_cast<const uint4*>(vs + k * (kRank * 2));
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&vempty[slot]);
+        }
+        if (broken) continue;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int tk = (ch + (k >> 2)) * kVTok + e * 4 + (k & 3);   // token index within the tile
+          if (t0 + tk < t_end) {
+            float h[8];
+            unpack8<VT>(u[k], h);
+            const float2 p = pbuf[tk];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              acc0[c] = fmaf(p.x, h[c], acc0[c]);
+              acc1[c] = fmaf(p.y, h[c], acc1[c]);
+            }
+          }
+        }
+      }
+    }
+
+    // reduce the four warps' partial sums and write this split's partials
+    aborted = tc::named_bar_or(kBarPv, kWgThreads, aborted || broken || *abort_flag != 0);
+    if (!aborted) {
+      const float ls0 = warp_sum(l0), ls1 = warp_sum(l1);
+      if (lane == 0) lred[e] = make_float2(ls0, ls1);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        ored[(e * kHeads + 0) * kRank + lane * 8 + c] = acc0[c];
+        ored[(e * kHeads + 1) * kRank + lane * 8 + c] = acc1[c];
+      }
+      tc::named_bar(kBarPv, kWgThreads);
+      for (int idx = ei; idx < kHeads * kRank; idx += kWgThreads) {
+        const int j = idx / kRank, c = idx % kRank;
+        float o = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) o += ored[(k * kHeads + j) * kRank + c];
+        const int64_t bh = (int64_t)b * a.n_heads + head0 + j;
+        a.part_o[(bh * a.n_splits + split) * kRank + c] = o;
+      }
+      if (ei < kHeads) {
+        float L = 0.f;
+        for (int k = 0; k < 4; ++k) L += (ei == 0) ? lred[k].x : lred[k].y;
+        const int64_t bh = (int64_t)b * a.n_heads + head0 + ei;
+        a.part_ml[bh * a.n_splits + split] = make_float2(ei == 0 ? m_run0 : m_run1, L);
+      }
+    }
+  }
+
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  if (threadIdx.x == 0 && *abort_flag) record_error(a.err, kCodeTimeout, kErrWait, blockIdx.x, b);
+  if (warp == 1) tc::tmem_dealloc(tmem_base, kTmemCols);
+}
+
+// ---------------------------------------------------------------------------- host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const cuuint64_t* dims,
+            const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle sw) {
+  const cuuint32_t es[3] = {1, 1, 1};
+  return encode_fn()(m, dt, rank, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool tc_supported(const DecodeArgs& a) {
+  return (a.k_dtype == kF16 || a.k_dtype == kBF16) && a.v_dtype == a.k_dtype && a.dh == kDh && a.rk == kRank &&
+         a.rv == kRank && a.s % kHeads == 0 && (int64_t)a.batch * a.capacity >= kTile &&
+         (int64_t)a.batch * a.capacity < (int64_t(1) << 31) && encode_fn() != nullptr;
+}
+
+int tc_tile_tokens() { return kTile; }
+int tc_ctas_per_group(const DecodeArgs& a) { return a.s / kHeads; }
+
+cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st) {
+  if (!encode_fn()) return cudaErrorNotSupported;
+  const CUtensorMapDataType dt = a.k_dtype == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUtensorMap tm_hk, tm_hv, tm_b;
+  const cuuint64_t rows = (cuuint64_t)a.batch * a.capacity;
+  {
+    // H_k as [rows][n_g][r]: boxes of 64 ranks x 1 group x 128 tokens, 128-byte swizzle (MMA operand)
+    const cuuint64_t dims[3] = {(cuuint64_t)a.rk, (cuuint64_t)a.n_g, rows};
+    const cuuint64_t strides[2] = {(cuuint64_t)a.rk * 2, (cuuint64_t)a.n_g * a.rk * 2};
+    const cuuint32_t box[3] = {kKChunk, 1, kTile};
+    if (!encode(&tm_hk, dt, 3, a.hk, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+  }
+  {
+    // H_v as [rows][n_g][r]: boxes of whole 512-byte rows x 32 tokens, unswizzled (row reads)
+    const cuuint64_t dims[3] = {(cuuint64_t)a.rv, (cuuint64_t)a.n_g, rows};
+    const cuuint64_t strides[2] = {(cuuint64_t)a.rv * 2, (cuuint64_t)a.n_g * a.rv * 2};
+    const cuuint32_t box[3] = {(cuuint32_t)kRank, 1, kVTok};
+    if (!encode(&tm_hv, dt, 3, a.hv, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE)) return cudaErrorInvalidValue;
+  }
+  {
+    // B_k^T as [n_g * s * d_h][r]: boxes of 64 ranks x 256 rows, 128-byte swizzle
+    const cuuint64_t dims[2] = {(cuuint64_t)a.rk, (cuuint64_t)a.n_g * a.s * a.dh};
+    const cuuint64_t strides[1] = {(cuuint64_t)a.rk * 2};
+    const cuuint32_t box[2] = {kKChunk, kN};
+    if (!encode(&tm_b, dt, 2, a.bkt, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+  }
+  TcParams P;
+  P.a = a;
+  P.hp_count = a.s / kHeads;
+  P.bf16 = a.k_dtype == kBF16;
+  dim3 grid(a.n_splits * P.hp_count, a.n_g, a.batch);
+  cudaError_t e;
+  if (a.k_dtype == kBF16) {
+    e = cudaFuncSetAttribute(decode_tc_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+    if (e != cudaSuccess) return e;
+    decode_tc_kernel<__nv_bfloat16><<<grid, kThreads, kSmemAlloc, st>>>(tm_hk, tm_hv, tm_b, P);
+  } else {
+    e = cudaFuncSetAttribute(decode_tc_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+    if (e != cudaSuccess) return e;
+    decode_tc_kernel<__half><<<grid, kThreads, kSmemAlloc, st>>>(tm_hk, tm_hv, tm_b, P);
+  }
+  return cudaGetLastError();
+}
 
 }  // namespace palu

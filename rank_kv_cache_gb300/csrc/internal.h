@@ -30,6 +30,12 @@ struct DecodeArgs {
   const void* bk;             // [n_g][rk][s*dh], bk_dtype
   const void* bkt;            // [n_g][s*dh][rk], MMA dtype (K-major operand for tcgen05)
   const float2* rope;         // [max_pos][dh/2] (cos, sin)
+  const uint64_t* phase;      // [dh/2] frequency of each pair as a 64-bit fraction of a turn
+  // query (read directly by kernels that rotate it themselves)
+  const void* q;
+  int q_dtype;
+  const int32_t* q_pos;       // nullable
+  float qscale;               // log2(e) / sqrt(dh)
   // split-T partials
   float* part_o;              // [B][n][n_splits][rv]
   float2* part_ml;            // [B][n][n_splits] (running max m in log2 units, sum l)
@@ -39,7 +45,7 @@ struct DecodeArgs {
 };
 
 // create-time set-up
-cudaError_t launch_rope_table(float2* tab, int64_t max_pos, int dh, double theta, cudaStream_t st);
+cudaError_t launch_rope_table(float2* tab, uint64_t* phase, int64_t max_pos, int dh, double theta, cudaStream_t st);
 cudaError_t launch_copy_bk(const void* src, int bk_dtype, void* dst, void* dst_t, int mma_dtype, int n_g,
                            int rk, int cols, cudaStream_t st);
 
@@ -57,6 +63,7 @@ cudaError_t launch_debug_dequant(const void* cache, const __half* scale, int cac
 // tcgen05 rebuild path (decode_tc.cu); returns cudaErrorNotSupported when the shape has no kernel
 bool tc_supported(const DecodeArgs& a);
 int tc_tile_tokens();
+int tc_ctas_per_group(const DecodeArgs& a);
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st);
 
 constexpr int kSimtTile = 16;   // tokens per SIMT tile

@@ -18,7 +18,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 int elem_bytes(palu_dtype_t t) { return t == PALU_F32 ? 4 : 2; }
 
 struct WsLayout {
-  size_t err, bk, bkt, rope, qbuf, part_o, part_ml, total;
+  size_t err, bk, bkt, rope, phase, qbuf, part_o, part_ml, total;
   int max_splits;
   int64_t max_pos;
 };
@@ -63,6 +63,8 @@ WsLayout layout_of(const palu_attn_desc& d) {
   if (d.mode == PALU_MODE_ROPE && d.k_dtype != PALU_F32) off = align256(off + (size_t)n_g * cols * d.rank_k * 2);
   L.rope = off;
   if (d.mode == PALU_MODE_ROPE) off = align256(off + (size_t)L.max_pos * (d.head_dim / 2) * sizeof(float2));
+  L.phase = off;
+  if (d.mode == PALU_MODE_ROPE) off = align256(off + (size_t)(d.head_dim / 2) * sizeof(uint64_t));
   const int qw = d.mode == PALU_MODE_ROPE ? d.head_dim : d.rank_k;
   L.qbuf = off;
   off = align256(off + (size_t)d.max_batch * d.n_heads * qw * sizeof(float));
@@ -75,6 +77,31 @@ WsLayout layout_of(const palu_attn_desc& d) {
 }
 
 int to_dt(palu_dtype_t t) { return (int)t; }
+
+// Split-T plan. `slots` CTAs run at once; each unit (one CTA's share of a group) is cut
+// into `splits` ranges of `tps` tiles. Picks the split count with the smallest estimated
+// time waves * (tps + 1), where the +1 stands for a CTA's fixed cost (operand load,
+// partial write), which also keeps splits from growing without need.
+void plan_splits(int64_t tiles, int64_t units, int64_t slots, int64_t max_splits, int* n_splits, int* tps_out) {
+  int64_t cap = tiles < max_splits ? tiles : max_splits;
+  if (cap < 1) cap = 1;
+  double best = 1e300;
+  int64_t best_s = 1, best_t = tiles;
+  for (int64_t s = 1; s <= cap; ++s) {
+    const int64_t tps = (tiles + s - 1) / s;
+    const int64_t s2 = (tiles + tps - 1) / tps;
+    if (s2 != s) continue;  // same plan as a smaller split count
+    const int64_t waves = (units * s2 + slots - 1) / slots;
+    const double est = double(waves) * double(tps + 1);
+    if (est < best - 1e-9) {
+      best = est;
+      best_s = s2;
+      best_t = tps;
+    }
+  }
+  *n_splits = (int)best_s;
+  *tps_out = (int)best_t;
+}
 
 }  // namespace
 
@@ -158,7 +185,8 @@ palu_status_t palu_attn_create(const palu_attn_desc* desc, const void* B_k, void
   if (e == cudaSuccess)
     e = launch_copy_bk(B_k, to_dt(desc->bk_dtype), h->ws + L.bk, bkt, h->mma_dtype, h->n_g, desc->rank_k, cols, s);
   if (e == cudaSuccess && desc->mode == PALU_MODE_ROPE)
-    e = launch_rope_table(reinterpret_cast<float2*>(h->ws + L.rope), L.max_pos, desc->head_dim, desc->rope_theta, s);
+    e = launch_rope_table(reinterpret_cast<float2*>(h->ws + L.rope), reinterpret_cast<uint64_t*>(h->ws + L.phase),
+                          L.max_pos, desc->head_dim, desc->rope_theta, s);
   if (e != cudaSuccess) {
     delete h;
     return PALU_ERR_CUDA;
@@ -307,6 +335,11 @@ palu_status_t palu_decode_attn(palu_attn_t h, const void* q, const palu_cache* c
   a.bk = h->ws + h->L.bk;
   a.bkt = h->ws + h->L.bkt;
   a.rope = reinterpret_cast<const float2*>(h->ws + h->L.rope);
+  a.phase = reinterpret_cast<const uint64_t*>(h->ws + h->L.phase);
+  a.q = q;
+  a.q_dtype = to_dt(d.q_dtype);
+  a.q_pos = q_pos;
+  a.qscale = float(1.4426950408889634 / sqrt((double)d.head_dim));
   a.part_o = reinterpret_cast<float*>(h->ws + h->L.part_o);
   a.part_ml = reinterpret_cast<float2*>(h->ws + h->L.part_ml);
   a.err = reinterpret_cast<ErrWord*>(h->ws + h->L.err);
@@ -314,21 +347,14 @@ palu_status_t palu_decode_attn(palu_attn_t h, const void* q, const palu_cache* c
   const int mode = d.mode == PALU_MODE_ROPE ? kRope : kAbsorbed;
   const bool use_tc = mode == kRope && tc_supported(a);
   const int tile = use_tc ? tc_tile_tokens() : kSimtTile;
-  // split-T plan: enough CTAs to cover the SMs about twice
   const int64_t tiles = max_seq_len > 0 ? (max_seq_len + tile - 1) / tile : 1;
-  const int64_t units = (int64_t)batch * h->n_g;
-  const int64_t target = 2LL * h->sm_count;
-  int64_t splits = (target + units - 1) / units;
-  const int64_t cap = tiles < h->L.max_splits ? tiles : h->L.max_splits;
-  if (splits > cap) splits = cap;
-  if (splits < 1) splits = 1;
-  const int64_t tps = (tiles + splits - 1) / splits;
-  splits = (tiles + tps - 1) / tps;
-  a.n_splits = (int)splits;
-  a.tiles_per_split = (int)tps;
+  const int64_t units = (int64_t)batch * h->n_g * (use_tc ? tc_ctas_per_group(a) : 1);
+  plan_splits(tiles, units, use_tc ? h->sm_count : 2 * h->sm_count, h->L.max_splits, &a.n_splits,
+              &a.tiles_per_split);
 
-  const float qscale = float(1.4426950408889634 / sqrt((double)d.head_dim));
-  cudaError_t e = launch_qprep(mode, q, to_dt(d.q_dtype), a, q_pos, qscale, const_cast<float*>(a.qbuf), s);
+  // the tensor-core kernel rotates its query itself; the other kernels read the prepared buffer
+  cudaError_t e = use_tc ? cudaSuccess
+                         : launch_qprep(mode, q, to_dt(d.q_dtype), a, q_pos, a.qscale, const_cast<float*>(a.qbuf), s);
   cudaEvent_t* tr = (e == cudaSuccess) ? trace_slot(h) : nullptr;
   if (tr) e = cudaEventRecord(tr[0], s);
   if (e == cudaSuccess) e = use_tc ? launch_decode_tc(a, s) : launch_decode_simt(mode, a, s);

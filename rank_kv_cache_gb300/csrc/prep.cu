@@ -10,7 +10,10 @@ namespace palu {
 // RoPE table: tab[p][k] = (cos(p w_k), sin(p w_k)), w_k = theta^(-2k/d_h), computed in
 // float64 and rounded to float32 once (rotate-half RoPE with the RoFormer schedule).
 // ---------------------------------------------------------------------------
-__global__ void rope_table_kernel(float2* tab, int64_t max_pos, int half, int dh, double theta) {
+// Also phase[k] = frac(w_k / 2pi) as a 64-bit fixed-point fraction of a turn, so that the
+// phase of position p is the top bits of p * phase[k] mod 2^64 (phase accumulation as in
+// direct digital synthesis): exact integer range reduction for every position.
+__global__ void rope_table_kernel(float2* tab, uint64_t* phase, int64_t max_pos, int half, int dh, double theta) {
   const int64_t n = max_pos * half;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t p = i / half;
@@ -19,13 +22,18 @@ __global__ void rope_table_kernel(float2* tab, int64_t max_pos, int half, int dh
     double sn, cs;
     sincos(double(p) * w, &sn, &cs);
     tab[i] = make_float2(float(cs), float(sn));
+    if (p == 0) {
+      const double turns = w / 6.283185307179586476925286766559;
+      const double v = ldexp(turns - floor(turns), 64);
+      phase[k] = v >= 18446744073709549568.0 ? ~0ull : __double2ull_rn(v);
+    }
   }
 }
 
-cudaError_t launch_rope_table(float2* tab, int64_t max_pos, int dh, double theta, cudaStream_t st) {
+cudaError_t launch_rope_table(float2* tab, uint64_t* phase, int64_t max_pos, int dh, double theta, cudaStream_t st) {
   const int64_t n = max_pos * (dh / 2);
   const int blocks = int((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
-  rope_table_kernel<<<blocks, 256, 0, st>>>(tab, max_pos, dh / 2, dh, theta);
+  rope_table_kernel<<<blocks, 256, 0, st>>>(tab, phase, max_pos, dh / 2, dh, theta);
   return cudaGetLastError();
 }
 
