@@ -462,10 +462,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) tc::mbar_arrive(&vempty[slot]);
         }
         if (broken) continue;
+        // all eight tokens valid (every tile but the last): no per-token branch
+        const bool all = t0 + (ch + 1) * kVTok + e * 4 + 3 < t_end;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const int tk = (ch + (k >> 2)) * kVTok + e * 4 + (k & 3);   // token index within the tile
-          if (t0 + tk < t_end) {
+          if (all || t0 + tk < t_end) {
             float h[8];
             unpack8<VT>(u[k], h);
             const float2 p = pbuf[tk];
