@@ -66,6 +66,11 @@ int tc_tile_tokens();
 int tc_ctas_per_group(const DecodeArgs& a);
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st);
 
+// TMA-streaming absorbed-mode kernel (decode_abs.cu)
+bool abs_supported(const DecodeArgs& a);
+int abs_stage_tokens();
+cudaError_t launch_decode_abs(const DecodeArgs& a, cudaStream_t st);
+
 constexpr int kSimtTile = 16;   // tokens per SIMT tile
 
 }  // namespace palu

@@ -345,11 +345,14 @@ palu_status_t palu_decode_attn(palu_attn_t h, const void* q, const palu_cache* c
   a.err = reinterpret_cast<ErrWord*>(h->ws + h->L.err);
 
   const int mode = d.mode == PALU_MODE_ROPE ? kRope : kAbsorbed;
+  // kernel choice: tensor-core rebuild (RoPE, fp16/bf16), TMA stream (absorbed, fp16/bf16),
+  // CUDA-core kernel for everything else (fp32 and int4 latents, other shapes)
   const bool use_tc = mode == kRope && tc_supported(a);
-  const int tile = use_tc ? tc_tile_tokens() : kSimtTile;
+  const bool use_abs = mode == kAbsorbed && abs_supported(a);
+  const int tile = use_tc ? tc_tile_tokens() : use_abs ? abs_stage_tokens() : kSimtTile;
   const int64_t tiles = max_seq_len > 0 ? (max_seq_len + tile - 1) / tile : 1;
   const int64_t units = (int64_t)batch * h->n_g * (use_tc ? tc_ctas_per_group(a) : 1);
-  plan_splits(tiles, units, use_tc ? h->sm_count : 2 * h->sm_count, h->L.max_splits, &a.n_splits,
+  plan_splits(tiles, units, (use_tc || use_abs) ? h->sm_count : 2 * h->sm_count, h->L.max_splits, &a.n_splits,
               &a.tiles_per_split);
 
   // the tensor-core kernel rotates its query itself; the other kernels read the prepared buffer
@@ -357,7 +360,8 @@ palu_status_t palu_decode_attn(palu_attn_t h, const void* q, const palu_cache* c
                          : launch_qprep(mode, q, to_dt(d.q_dtype), a, q_pos, a.qscale, const_cast<float*>(a.qbuf), s);
   cudaEvent_t* tr = (e == cudaSuccess) ? trace_slot(h) : nullptr;
   if (tr) e = cudaEventRecord(tr[0], s);
-  if (e == cudaSuccess) e = use_tc ? launch_decode_tc(a, s) : launch_decode_simt(mode, a, s);
+  if (e == cudaSuccess)
+    e = use_tc ? launch_decode_tc(a, s) : use_abs ? launch_decode_abs(a, s) : launch_decode_simt(mode, a, s);
   if (tr && e == cudaSuccess) e = cudaEventRecord(tr[1], s);
   if (e == cudaSuccess) e = launch_combine(a, out, lse, s);
   return e == cudaSuccess ? PALU_OK : PALU_ERR_CUDA;
