@@ -8,18 +8,19 @@
 //   * one (batch row b, group g, head pair hp, T-split) unit; the head pair's
 //     slice of B_k^T (256 rows x r, K-major) stays in shared memory;
 //   * warp 0 streams 128-token x 64-rank chunks of H_k,g by TMA (128-byte swizzle)
-//     through a 3-stage ring; warp 10 streams 16-token chunks of H_v,g by TMA
+//     through a 3-stage ring; warp 2 streams 16-token chunks of H_v,g by TMA
 //     through a 5-slot ring;
 //   * warp 1 issues tcgen05.mma (M=128 tokens, N=256 = 2 heads x d_h, K=r) into
 //     one of two TMEM accumulators;
-//   * the score warpgroup (warps 2-5, one token row per thread, read with
-//     tcgen05.ld) rotates every rebuilt key pair at the token's position and dots
-//     it with the rotated query, writing the tile's scores to a double-buffered
-//     slot in shared memory;
-//   * the softmax warpgroup (warps 6-9) runs the online softmax (base 2) on the
-//     previous tile's scores and accumulates p H_v in latent space on CUDA cores,
-//     so scoring and p H_v of consecutive tiles overlap; the T-split partials go
-//     to the merge kernel.
+//   * two score warpgroups (one token row per thread, read with tcgen05.ld; each
+//     takes half of the 64 rotation pairs) rotate every rebuilt key pair at the
+//     token's position and dot it with the rotated query, leaving partial scores
+//     of the tile in a double-buffered slot in shared memory;
+//   * two softmax warpgroups run the same online softmax (base 2) on the previous
+//     tile's scores and each accumulates p H_v for half of the value-latent
+//     columns on CUDA cores, so scoring and p H_v of consecutive tiles overlap;
+//     the T-split partials go to the merge kernel.
+//   * setmaxnreg moves registers from the control warpgroup to the score warpgroups.
 // RoPE angles: pair k's frequency is held as a 64-bit fixed-point fraction of a
 // turn F_k, so position p's phase is (p * F_k mod 2^64) / 2^64 turns: integer
 // range reduction with no rounding (phase accumulation as in direct digital
@@ -53,11 +54,16 @@ constexpr int kVTok = 16;                        // tokens per H_v chunk
 constexpr int kVChunks = kTile / kVTok;          // 8 per tile
 constexpr int kVSlots = 5;                       // H_v ring
 constexpr int kVSlot = kVTok * kRank * 2;        // 8 KB
-constexpr int kWgThreads = 128;                  // one warpgroup
-// warps: 0 H_k/B producer, 1 MMA issuer, 2-5 score warpgroup, 6-9 softmax/PV warpgroup, 10 H_v producer
-constexpr int kThreads = 11 * 32;
-constexpr int kBarScore = 1;                     // named barrier of the score warpgroup
-constexpr int kBarPv = 2;                        // named barrier of the softmax/PV warpgroup
+constexpr int kVHalf = kRank / 2;                // value columns per softmax/PV warpgroup
+constexpr int kWg = 128;                         // threads per warpgroup
+// Warpgroups: 0 = warp 0 H_k/B producer, warp 1 MMA issuer, warp 2 H_v producer, warp 3 idle;
+// 1, 2 = score warpgroups (rotation pairs 0-31 / 32-63); 3, 4 = softmax/PV warpgroups
+// (value columns 0-127 / 128-255).
+constexpr int kThreads = 5 * kWg;
+// Registers per thread after setmaxnreg; 128*48 + 256*152 + 256*64 = 61440 = 640 threads x
+// the 96 registers each thread is launched with (launch bounds 640 threads, one CTA per SM).
+constexpr int kRegsCtl = 48, kRegsScore = 152, kRegsPv = 64;
+static_assert(kWg * kRegsCtl + 2 * kWg * kRegsScore + 2 * kWg * kRegsPv <= kThreads * 96, "register split");
 constexpr uint32_t kTmemCols = 512;              // two N=256 fp32 accumulators
 constexpr uint64_t kWaitNs = 1000000000ull;      // 1 s per wait
 constexpr float kTurnToRad = 1.4629180792671596e-09f;  // 2 pi / 2^32
@@ -72,14 +78,14 @@ constexpr int kNumBars = 2 * kStages + kChunks + 2 + 2 + 2 * kVSlots + 2 + 2 + 1
 constexpr int kOffMisc = kOffBar + 8 * kNumBars;
 constexpr int kOffQ = (kOffMisc + 16 + 15) & ~15;           // float4 [kHalf]: (qa0, qa1, qb0, qb1)
 constexpr int kOffF = kOffQ + kHalf * 16;                   // uint64 [kHalf]
-constexpr int kOffS = kOffF + kHalf * 8;                    // float2 [2][kTile] scores
-constexpr int kOffRed = kOffS + 2 * kTile * 8;              // float2 [4]
-constexpr int kOffP = kOffRed + 4 * 8;                      // float2 [kTile]
-constexpr int kOffL = kOffP + kTile * 8;                    // float2 [4]
-constexpr int kSmemBytes = kOffL + 4 * 8;
+constexpr int kOffS = kOffF + kHalf * 8;                    // float2 [2 buf][2 part][kTile] partial scores
+constexpr int kOffRed = kOffS + 4 * kTile * 8;              // float2 [2 wg][4]
+constexpr int kOffP = kOffRed + 2 * 4 * 8;                  // float2 [2 wg][kTile]
+constexpr int kOffL = kOffP + 2 * kTile * 8;                // float2 [2 wg][4]
+constexpr int kSmemBytes = kOffL + 2 * 4 * 8;
 constexpr int kSmemAlloc = kSmemBytes + 1024;
-constexpr int kOffO = kOffV;                                // float [4][kHeads][kRank], reuses the H_v ring
-static_assert(4 * kHeads * kRank * 4 <= kVSlots * kVSlot, "output reduction fits the H_v ring");
+constexpr int kOffO = kOffV;                                // float [2 wg][4][kHeads][kVHalf], reuses the H_v ring
+static_assert(2 * 4 * kHeads * kVHalf * 4 <= kVSlots * kVSlot, "output reduction fits the H_v ring");
 static_assert(kSmemAlloc <= 232448, "shared memory budget");
 
 struct TcParams {
@@ -89,25 +95,22 @@ struct TcParams {
 };
 
 template <typename VT>
-__device__ __forceinline__ void unpack8(const uint4& u, float* h);
+__device__ __forceinline__ void unpack4(const uint2& u, float* h);
 template <>
-__device__ __forceinline__ void unpack8<__half>(const uint4& u, float* h) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
-    h[2 * i] = f.x;
-    h[2 * i + 1] = f.y;
-  }
+__device__ __forceinline__ void unpack4<__half>(const uint2& u, float* h) {
+  const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+  const float2 y = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+  h[0] = x.x;
+  h[1] = x.y;
+  h[2] = y.x;
+  h[3] = y.y;
 }
 template <>
-__device__ __forceinline__ void unpack8<__nv_bfloat16>(const uint4& u, float* h) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    h[2 * i] = __uint_as_float(w[i] << 16);
-    h[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-  }
+__device__ __forceinline__ void unpack4<__nv_bfloat16>(const uint2& u, float* h) {
+  h[0] = __uint_as_float(u.x << 16);
+  h[1] = __uint_as_float(u.x & 0xffff0000u);
+  h[2] = __uint_as_float(u.y << 16);
+  h[3] = __uint_as_float(u.y & 0xffff0000u);
 }
 
 __device__ __forceinline__ int token_position(const DecodeArgs& a, int b, int t, bool valid) {
@@ -120,6 +123,15 @@ __device__ __forceinline__ int token_position(const DecodeArgs& a, int b, int t,
   return pos;
 }
 
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 template <typename VT>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_hk, const __grid_constant__ CUtensorMap tm_hv,
@@ -128,6 +140,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const DecodeArgs& a = P.a;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wg = threadIdx.x / kWg;
   const int hp = blockIdx.x % P.hp_count, split = blockIdx.x / P.hp_count;
   const int g = blockIdx.y, b = blockIdx.z;
 
@@ -147,10 +160,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   float4* qs = reinterpret_cast<float4*>(smem + kOffQ);
   uint64_t* Fs = reinterpret_cast<uint64_t*>(smem + kOffF);
   float2* sbuf = reinterpret_cast<float2*>(smem + kOffS);
-  float2* red = reinterpret_cast<float2*>(smem + kOffRed);
-  float2* pbuf = reinterpret_cast<float2*>(smem + kOffP);
-  float* ored = reinterpret_cast<float*>(smem + kOffO);
-  float2* lred = reinterpret_cast<float2*>(smem + kOffL);
 
   // this CTA's token range
   int T = a.seq_lens[b];
@@ -173,13 +182,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kChunks; ++i) tc::mbar_init(&bfull[i], 1);
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&tfull[i], 1);
-      tc::mbar_init(&tempty[i], 4);
-      tc::mbar_init(&sready[i], 4);
-      tc::mbar_init(&sfree[i], 4);
+      tc::mbar_init(&tempty[i], 8);   // lane 0 of the eight score warps
+      tc::mbar_init(&sready[i], 8);   // eight score warps
+      tc::mbar_init(&sfree[i], 8);    // eight softmax/PV warps
     }
     for (int i = 0; i < kVSlots; ++i) {
       tc::mbar_init(&vfull[i], 1);
-      tc::mbar_init(&vempty[i], 4);
+      tc::mbar_init(&vempty[i], 8);   // eight softmax/PV warps
     }
     tc::mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -189,10 +198,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::tmem_alloc(tmem_slot, kTmemCols);
     tc::tmem_relinquish();
   }
-  if (warp >= 2 && warp < 6) {
+  if (wg == 1) {
     // rotate the two heads' queries at q_pos (RoPE table, float64-derived), scale by
     // log2(e)/sqrt(d_h), and keep them as (q_a, q_b) pairs per rotation pair
-    const int i = threadIdx.x - 64;
+    const int i = threadIdx.x - kWg;
     const int j = i / kHalf, k = i % kHalf;
     int qp = 0;
     if (a.q_pos) qp = a.q_pos[b];
@@ -215,126 +224,132 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ H_k / B producer
-    if (lane == 0 && n_tiles > 0) {
-      tc::tma_prefetch(&tm_hk);
-      tc::tma_prefetch(&tm_b);
-      const int brow = g * (a.s * kDh) + hp * kN;
-      for (int kc = 0; kc < kChunks; ++kc) {
-        tc::mbar_arrive_expect_tx(&bfull[kc], kBChunk);
-        tc::tma_load_2d(smem + kOffB + kc * kBChunk, &tm_b, &bfull[kc], kc * kKChunk, brow);
-      }
-      int stage = 0, issued = 0;
-      uint32_t round = 0;
-      bool ok = true;
-      for (int it = 0; it < n_tiles && ok; ++it) {
-        const int t0 = t_begin + it * kTile;
+  if (wg == 0) {
+    setmaxnreg_dec<kRegsCtl>();
+    if (warp == 0) {
+      // ---------------------------------------------------------- H_k / B producer
+      if (lane == 0 && n_tiles > 0) {
+        tc::tma_prefetch(&tm_hk);
+        tc::tma_prefetch(&tm_b);
+        const int brow = g * (a.s * kDh) + hp * kN;
         for (int kc = 0; kc < kChunks; ++kc) {
-          if (!tc::mbar_wait_bounded(&emptyA[stage], (round & 1) ^ 1, abort_flag, kWaitNs)) {
-            ok = false;
-            break;
-          }
-          tc::mbar_arrive_expect_tx(&fullA[stage], kAStage);
-          tc::tma_load_3d(smem + kOffA + stage * kAStage, &tm_hk, &fullA[stage], kc * kKChunk, g, row0 + t0);
-          ++issued;
-          if (++stage == kStages) {
-            stage = 0;
-            ++round;
+          tc::mbar_arrive_expect_tx(&bfull[kc], kBChunk);
+          tc::tma_load_2d(smem + kOffB + kc * kBChunk, &tm_b, &bfull[kc], kc * kKChunk, brow);
+        }
+        int stage = 0, issued = 0;
+        uint32_t round = 0;
+        bool ok = true;
+        for (int it = 0; it < n_tiles && ok; ++it) {
+          const int t0 = t_begin + it * kTile;
+          for (int kc = 0; kc < kChunks; ++kc) {
+            if (!tc::mbar_wait_bounded(&emptyA[stage], (round & 1) ^ 1, abort_flag, kWaitNs)) {
+              ok = false;
+              break;
+            }
+            tc::mbar_arrive_expect_tx(&fullA[stage], kAStage);
+            tc::tma_load_3d(smem + kOffA + stage * kAStage, &tm_hk, &fullA[stage], kc * kKChunk, g, row0 + t0);
+            ++issued;
+            if (++stage == kStages) {
+              stage = 0;
+              ++round;
+            }
           }
         }
-      }
-      if (!ok) {
-        // drain the copies still in flight before the CTA may exit
-        volatile int quiet = 0;
-        for (int k = 0, s = stage, r = (int)round; k < (issued < kStages ? issued : kStages); ++k) {
-          if (--s < 0) {
-            s = kStages - 1;
-            --r;
+        if (!ok) {
+          // drain the copies still in flight before the CTA may exit
+          volatile int quiet = 0;
+          for (int k = 0, s = stage, r = (int)round; k < (issued < kStages ? issued : kStages); ++k) {
+            if (--s < 0) {
+              s = kStages - 1;
+              --r;
+            }
+            tc::mbar_wait_bounded(&fullA[s], uint32_t(r) & 1, &quiet, kWaitNs / 10);
           }
-          tc::mbar_wait_bounded(&fullA[s], uint32_t(r) & 1, &quiet, kWaitNs / 10);
-        }
-        for (int kc = 0; kc < kChunks; ++kc) tc::mbar_wait_bounded(&bfull[kc], 0, &quiet, kWaitNs / 10);
-      }
-    }
-  } else if (warp == 10) {
-    // ------------------------------------------------------------ H_v producer
-    if (lane == 0 && n_tiles > 0) {
-      tc::tma_prefetch(&tm_hv);
-      int issued = 0;
-      bool ok = true;
-      for (int it = 0; it < n_tiles && ok; ++it) {
-        const int t0 = t_begin + it * kTile;
-        for (int ch = 0; ch < kVChunks; ++ch) {
-          const int vi = it * kVChunks + ch;
-          const int slot = vi % kVSlots;
-          if (!tc::mbar_wait_bounded(&vempty[slot], ((vi / kVSlots) & 1) ^ 1, abort_flag, kWaitNs)) {
-            ok = false;
-            break;
-          }
-          tc::mbar_arrive_expect_tx(&vfull[slot], kVSlot);
-          tc::tma_load_3d(smem + kOffV + slot * kVSlot, &tm_hv, &vfull[slot], 0, g, row0 + t0 + ch * kVTok);
-          ++issued;
+          for (int kc = 0; kc < kChunks; ++kc) tc::mbar_wait_bounded(&bfull[kc], 0, &quiet, kWaitNs / 10);
         }
       }
-      if (!ok) {
-        volatile int quiet = 0;
-        for (int vi = (issued > kVSlots ? issued - kVSlots : 0); vi < issued; ++vi)
-          tc::mbar_wait_bounded(&vfull[vi % kVSlots], (vi / kVSlots) & 1, &quiet, kWaitNs / 10);
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n_tiles > 0) {
-      const uint32_t idesc = tc::idesc_f16(kTile, kN, P.bf16 != 0);
-      bool ok = true;
-      int stage = 0;
-      uint32_t round = 0;
-      const uint32_t a_base = tc::smem_addr(smem + kOffA);
-      const uint32_t b_base = tc::smem_addr(smem + kOffB);
-      for (int it = 0; it < n_tiles && ok; ++it) {
-        const int buf = it & 1;
-        const uint32_t use = it >> 1;
-        if (!tc::mbar_wait_bounded(&tempty[buf], (use & 1) ^ 1, abort_flag, kWaitNs)) {
-          ok = false;
-          break;
-        }
-        tc::tc_fence_after();
-        const uint32_t d = tmem_base + buf * kN;
-        for (int kc = 0; kc < kChunks; ++kc) {
-          if (it == 0 && !tc::mbar_wait_bounded(&bfull[kc], 0, abort_flag, kWaitNs)) {
-            ok = false;
-            break;
-          }
-          if (!tc::mbar_wait_bounded(&fullA[stage], round & 1, abort_flag, kWaitNs)) {
+    } else if (warp == 1) {
+      // ---------------------------------------------------------- MMA issuer
+      if (lane == 0 && n_tiles > 0) {
+        const uint32_t idesc = tc::idesc_f16(kTile, kN, P.bf16 != 0);
+        bool ok = true;
+        int stage = 0;
+        uint32_t round = 0;
+        const uint32_t a_base = tc::smem_addr(smem + kOffA);
+        const uint32_t b_base = tc::smem_addr(smem + kOffB);
+        for (int it = 0; it < n_tiles && ok; ++it) {
+          const int buf = it & 1;
+          const uint32_t use = it >> 1;
+          if (!tc::mbar_wait_bounded(&tempty[buf], (use & 1) ^ 1, abort_flag, kWaitNs)) {
             ok = false;
             break;
           }
           tc::tc_fence_after();
+          const uint32_t d = tmem_base + buf * kN;
+          for (int kc = 0; kc < kChunks; ++kc) {
+            if (it == 0 && !tc::mbar_wait_bounded(&bfull[kc], 0, abort_flag, kWaitNs)) {
+              ok = false;
+              break;
+            }
+            if (!tc::mbar_wait_bounded(&fullA[stage], round & 1, abort_flag, kWaitNs)) {
+              ok = false;
+              break;
+            }
+            tc::tc_fence_after();
 #pragma unroll
-          for (int k = 0; k < kKChunk / 16; ++k) {
-            const uint64_t ad = tc::sdesc_k_sw128(a_base + stage * kAStage + k * 32);
-            const uint64_t bd = tc::sdesc_k_sw128(b_base + kc * kBChunk + k * 32);
-            tc::umma_f16(d, ad, bd, idesc, (kc | k) != 0);
+            for (int k = 0; k < kKChunk / 16; ++k) {
+              const uint64_t ad = tc::sdesc_k_sw128(a_base + stage * kAStage + k * 32);
+              const uint64_t bd = tc::sdesc_k_sw128(b_base + kc * kBChunk + k * 32);
+              tc::umma_f16(d, ad, bd, idesc, (kc | k) != 0);
+            }
+            tc::umma_commit(&emptyA[stage]);
+            if (++stage == kStages) {
+              stage = 0;
+              ++round;
+            }
           }
-          tc::umma_commit(&emptyA[stage]);
-          if (++stage == kStages) {
-            stage = 0;
-            ++round;
+          if (!ok) break;
+          tc::umma_commit(&tfull[buf]);
+        }
+        // every MMA this thread issued has completed once mma_done flips
+        tc::umma_commit(mma_done);
+        volatile int quiet = 0;
+        tc::mbar_wait_bounded(mma_done, 0, &quiet, kWaitNs);
+      }
+    } else if (warp == 2) {
+      // ---------------------------------------------------------- H_v producer
+      if (lane == 0 && n_tiles > 0) {
+        tc::tma_prefetch(&tm_hv);
+        int issued = 0;
+        bool ok = true;
+        for (int it = 0; it < n_tiles && ok; ++it) {
+          const int t0 = t_begin + it * kTile;
+          for (int ch = 0; ch < kVChunks; ++ch) {
+            const int vi = it * kVChunks + ch;
+            const int slot = vi % kVSlots;
+            if (!tc::mbar_wait_bounded(&vempty[slot], ((vi / kVSlots) & 1) ^ 1, abort_flag, kWaitNs)) {
+              ok = false;
+              break;
+            }
+            tc::mbar_arrive_expect_tx(&vfull[slot], kVSlot);
+            tc::tma_load_3d(smem + kOffV + slot * kVSlot, &tm_hv, &vfull[slot], 0, g, row0 + t0 + ch * kVTok);
+            ++issued;
           }
         }
-        if (!ok) break;
-        tc::umma_commit(&tfull[buf]);
+        if (!ok) {
+          volatile int quiet = 0;
+          for (int vi = (issued > kVSlots ? issued - kVSlots : 0); vi < issued; ++vi)
+            tc::mbar_wait_bounded(&vfull[vi % kVSlots], (vi / kVSlots) & 1, &quiet, kWaitNs / 10);
+        }
       }
-      // every MMA this thread issued has completed once mma_done flips
-      tc::umma_commit(mma_done);
-      volatile int quiet = 0;
-      tc::mbar_wait_bounded(mma_done, 0, &quiet, kWaitNs);
     }
-  } else if (warp < 6) {
-    // ------------------------------------------------------------ score warpgroup
-    // thread = one token row of the tile: RoPE-rotate each rebuilt key pair at the
-    // token's position and dot it with the rotated query, for both heads.
+  } else if (wg <= 2) {
+    // ------------------------------------------------------------ score warpgroups
+    // thread = one token row of the tile; warpgroup X handles rotation pairs 32X..32X+31 of
+    // both heads: rotate each rebuilt key pair at the token's position, dot it with the
+    // rotated query, and leave the partial scores in shared memory.
+    setmaxnreg_inc<kRegsScore>();
+    const int X = wg - 1;
     const int quad = warp & 3;               // TMEM lane quadrant this warp may access
     const int row = quad * 32 + lane;
     int pos_next = token_position(a, b, t_begin + row, t_begin + row < t_end);
@@ -348,13 +363,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       const bool got = tc::mbar_wait_bounded(&tfull[buf], use & 1, abort_flag, kWaitNs) &&
                        tc::mbar_wait_bounded(&sfree[buf], (use & 1) ^ 1, abort_flag, kWaitNs);
-      if (tc::named_bar_or(kBarScore, kWgThreads, !got)) break;  // one decision for the warpgroup
+      if (tc::named_bar_or(1 + X, kWg, !got)) break;  // one decision for the warpgroup
       tc::tc_fence_after();
 
       float s0a = 0.f, s0b = 0.f, s1a = 0.f, s1b = 0.f;
       const uint32_t tbase = tmem_base + (uint32_t(quad * 32) << 16) + buf * kN;
 #pragma unroll 1
-      for (int a0 = 0; a0 < kHalf; a0 += 16) {
+      for (int a0 = 32 * X; a0 < 32 * X + 32; a0 += 16) {
         // issue the four TMEM loads of this chunk (pairs a0..a0+15 of both heads), compute
         // the chunk's cos/sin while they are in flight, then wait
         uint32_t k0[32], k1[32];
@@ -373,33 +388,43 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float4 q4 = qs[a0 + u];     // (qa0, qa1, qb0, qb1)
           const float ka0 = __uint_as_float(k0[u]), kb0 = __uint_as_float(k0[16 + u]);
           const float ka1 = __uint_as_float(k1[u]), kb1 = __uint_as_float(k1[16 + u]);
-          const float t0 = fmaf(q4.x, ka0, q4.z * kb0), v0 = fmaf(q4.z, ka0, -q4.x * kb0);
-          const float t1 = fmaf(q4.y, ka1, q4.w * kb1), v1 = fmaf(q4.w, ka1, -q4.y * kb1);
+          const float t0v = fmaf(q4.x, ka0, q4.z * kb0), v0 = fmaf(q4.z, ka0, -q4.x * kb0);
+          const float t1v = fmaf(q4.y, ka1, q4.w * kb1), v1 = fmaf(q4.w, ka1, -q4.y * kb1);
           if (u & 1) {
-            s0b = fmaf(sn[u], v0, fmaf(cs[u], t0, s0b));
-            s1b = fmaf(sn[u], v1, fmaf(cs[u], t1, s1b));
+            s0b = fmaf(sn[u], v0, fmaf(cs[u], t0v, s0b));
+            s1b = fmaf(sn[u], v1, fmaf(cs[u], t1v, s1b));
           } else {
-            s0a = fmaf(sn[u], v0, fmaf(cs[u], t0, s0a));
-            s1a = fmaf(sn[u], v1, fmaf(cs[u], t1, s1a));
+            s0a = fmaf(sn[u], v0, fmaf(cs[u], t0v, s0a));
+            s1a = fmaf(sn[u], v1, fmaf(cs[u], t1v, s1a));
           }
         }
       }
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&tempty[buf]);
-      sbuf[buf * kTile + row] = valid ? make_float2(s0a + s0b, s1a + s1b) : make_float2(-INFINITY, -INFINITY);
+      sbuf[(buf * 2 + X) * kTile + row] =
+          valid ? make_float2(s0a + s0b, s1a + s1b) : make_float2(-INFINITY, -INFINITY);
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&sready[buf]);
     }
   } else {
-    // ------------------------------------------------------------ softmax / PV warpgroup
-    const int e = warp - 6;                  // 0..3
-    const int ei = threadIdx.x - 6 * 32;     // 0..127: token row for the softmax
+    // ------------------------------------------------------------ softmax / PV warpgroups
+    // Both warpgroups run the same online softmax over the tile's 128 scores (summing the two
+    // partial scores); warpgroup Y accumulates p H_v for value columns 128Y..128Y+127.
+    setmaxnreg_dec<kRegsPv>();
+    const int Y = wg - 3;
+    const int e = warp & 3;                  // warp within the warpgroup
+    const int ei = threadIdx.x - wg * kWg;   // 0..127: token row for the softmax
+    const int bar = 3 + Y;
+    float2* red = reinterpret_cast<float2*>(smem + kOffRed) + Y * 4;
+    float2* pbuf = reinterpret_cast<float2*>(smem + kOffP) + Y * kTile;
+    float2* lred = reinterpret_cast<float2*>(smem + kOffL) + Y * 4;
+    float* ored = reinterpret_cast<float*>(smem + kOffO) + Y * (4 * kHeads * kVHalf);
     float m_run0 = -INFINITY, m_run1 = -INFINITY;
     float l0 = 0.f, l1 = 0.f;
-    float acc0[8], acc1[8];
+    float acc0[4], acc1[4];
 #pragma unroll
-    for (int c = 0; c < 8; ++c) acc0[c] = acc1[c] = 0.f;
+    for (int c = 0; c < 4; ++c) acc0[c] = acc1[c] = 0.f;
     bool aborted = false;  // warpgroup-uniform: only ever set from a barrier-OR
     bool broken = false;   // this warp's own H_v wait gave up
 
@@ -408,18 +433,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t use = it >> 1;
       const int t0 = t_begin + it * kTile;
       const bool got = tc::mbar_wait_bounded(&sready[buf], use & 1, abort_flag, kWaitNs);
-      if (tc::named_bar_or(kBarPv, kWgThreads, !got || broken)) {
+      if (tc::named_bar_or(bar, kWg, !got || broken)) {
         aborted = true;
         break;
       }
-      const float2 sc = sbuf[buf * kTile + ei];
+      const float2 pa = sbuf[(buf * 2 + 0) * kTile + ei];
+      const float2 pb = sbuf[(buf * 2 + 1) * kTile + ei];
+      const float2 sc = make_float2(pa.x + pb.x, pa.y + pb.y);
       __syncwarp();
-      if ((ei & 31) == 0) tc::mbar_arrive(&sfree[buf]);
+      if (lane == 0) tc::mbar_arrive(&sfree[buf]);
 
       // online softmax over the tile (uniform running max across the 128 threads)
       const float w0 = warp_max(sc.x), w1 = warp_max(sc.y);
       if (lane == 0) red[e] = make_float2(w0, w1);
-      tc::named_bar(kBarPv, kWgThreads);
+      tc::named_bar(bar, kWg);
       float tm0 = -INFINITY, tm1 = -INFINITY;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
@@ -436,28 +463,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       l0 = l0 * al0 + p0;
       l1 = l1 * al1 + p1;
       pbuf[ei] = make_float2(p0, p1);
-      tc::named_bar(kBarPv, kWgThreads);
+      tc::named_bar(bar, kWg);
 
-      // p H_v from the staged 16-token chunks; warp e takes 4 tokens of each chunk and
-      // lane owns columns 8*lane..8*lane+7
+      // p H_v over 16-token chunks; warp e takes 4 tokens of each chunk and lane owns
+      // columns 128Y + 4 lane .. 128Y + 4 lane + 3. A warp whose wait gave up skips the
+      // arithmetic; the tile-level barrier-OR above then ends the loop for the warpgroup.
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 0; c < 4; ++c) {
         acc0[c] *= al0;
         acc1[c] *= al1;
       }
-      // Waits here are bounded but not followed by a warpgroup barrier: a warp whose wait
-      // gave up skips the arithmetic and the tile-level decision above ends the loop for all.
       for (int ch = 0; ch < kVChunks; ch += 2) {
-        uint4 u[8];
+        uint2 u[8];
 #pragma unroll
         for (int c2 = 0; c2 < 2; ++c2) {
           const int vi = it * kVChunks + ch + c2;
           const int slot = vi % kVSlots;
-          const bool vgot = tc::mbar_wait_bounded(&vfull[slot], (vi / kVSlots) & 1, abort_flag, kWaitNs);
-          if (!vgot) broken = true;
-          const uint8_t* vs = smem + kOffV + slot * kVSlot + (e * 4) * (kRank * 2) + lane * 16;
+          if (!tc::mbar_wait_bounded(&vfull[slot], (vi / kVSlots) & 1, abort_flag, kWaitNs)) broken = true;
+          const uint8_t* vs = smem + kOffV + slot * kVSlot + (e * 4) * (kRank * 2) + (Y * kVHalf + lane * 4) * 2;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) u[c2 * 4 + k] = *reinterpret_cast<const uint4*>(vs + k * (kRank * 2));
+          for (int k = 0; k < 4; ++k) u[c2 * 4 + k] = *reinterpret_cast<const uint2*>(vs + k * (kRank * 2));
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(&vempty[slot]);
         }
@@ -468,11 +493,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < 8; ++k) {
           const int tk = (ch + (k >> 2)) * kVTok + e * 4 + (k & 3);   // token index within the tile
           if (all || t0 + tk < t_end) {
-            float h[8];
-            unpack8<VT>(u[k], h);
+            float h[4];
+            unpack4<VT>(u[k], h);
             const float2 p = pbuf[tk];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
+            for (int c = 0; c < 4; ++c) {
               acc0[c] = fmaf(p.x, h[c], acc0[c]);
               acc1[c] = fmaf(p.y, h[c], acc1[c]);
             }
@@ -482,25 +507,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // reduce the four warps' partial sums and write this split's partials
-    aborted = tc::named_bar_or(kBarPv, kWgThreads, aborted || broken || *abort_flag != 0);
+    aborted = tc::named_bar_or(bar, kWg, aborted || broken || *abort_flag != 0);
     if (!aborted) {
       const float ls0 = warp_sum(l0), ls1 = warp_sum(l1);
       if (lane == 0) lred[e] = make_float2(ls0, ls1);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        ored[(e * kHeads + 0) * kRank + lane * 8 + c] = acc0[c];
-        ored[(e * kHeads + 1) * kRank + lane * 8 + c] = acc1[c];
+      for (int c = 0; c < 4; ++c) {
+        ored[(e * kHeads + 0) * kVHalf + lane * 4 + c] = acc0[c];
+        ored[(e * kHeads + 1) * kVHalf + lane * 4 + c] = acc1[c];
       }
-      tc::named_bar(kBarPv, kWgThreads);
-      for (int idx = ei; idx < kHeads * kRank; idx += kWgThreads) {
-        const int j = idx / kRank, c = idx % kRank;
+      tc::named_bar(bar, kWg);
+      for (int idx = ei; idx < kHeads * kVHalf; idx += kWg) {
+        const int j = idx / kVHalf, c = idx % kVHalf;
         float o = 0.f;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) o += ored[(k * kHeads + j) * kRank + c];
+        for (int k = 0; k < 4; ++k) o += ored[(k * kHeads + j) * kVHalf + c];
         const int64_t bh = (int64_t)b * a.n_heads + head0 + j;
-        a.part_o[(bh * a.n_splits + split) * kRank + c] = o;
+        a.part_o[(bh * a.n_splits + split) * kRank + Y * kVHalf + c] = o;
       }
-      if (ei < kHeads) {
+      if (Y == 0 && ei < kHeads) {
         float L = 0.f;
         for (int k = 0; k < 4; ++k) L += (ei == 0) ? lred[k].x : lred[k].y;
         const int64_t bh = (int64_t)b * a.n_heads + head0 + ei;
