@@ -22,6 +22,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "split_merge.cuh"
 #include "tc_ptx.cuh"
 
 namespace palu {
@@ -287,6 +288,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   if (threadIdx.x == 0 && *abort_flag) record_error(a.err, kCodeTimeout, kErrWait, blockIdx.x, b);
+  merge_if_last(a, b, head0, kHeads, reinterpret_cast<volatile int*>(smem + kOffMisc + 4),
+                reinterpret_cast<float*>(smem + kOffRing));  // the ring is free by now
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,

@@ -3,7 +3,8 @@
 // One CTA per (split, group, batch row). It streams its T-range of the group's
 // latent rows in tiles of kSimtTile tokens, scores them for all s heads of the
 // group, keeps an online softmax per head and accumulates p H_v in latent space.
-// Output: split partials (m, l, o) that the merge kernel combines.
+// Output: split partials (m, l, o), merged by the last CTA of each unit (or by the merge
+// kernel when the caller provides no counters).
 //
 // RoPE mode ("Palu" notes, RoPE paragraph and the online-rebuild kernel paragraph):
 //   K[t] = H_k[t] B_k,g (all s heads at once), then for head j
@@ -12,6 +13,7 @@
 // Absorbed mode (key-fusion paragraph): score = q' . H_k[t] with q' = q B_k^T.
 // Queries arrive pre-scaled by log2(e)/sqrt(d_h); the softmax works in base 2.
 #include "internal.h"
+#include "split_merge.cuh"
 
 namespace palu {
 
@@ -192,6 +194,9 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(DecodeArgs a) {
     const int64_t bh = (int64_t)b * a.n_heads + g * s + tid;
     a.part_ml[bh * a.n_splits + split] = make_float2(st_s[tid], st_s[8 + tid]);
   }
+  __shared__ int merge_flag;
+  __syncthreads();  // the tile buffers are free: reuse them as merge scratch (s * (n_splits + 2) floats)
+  merge_if_last(a, b, g * s, s, &merge_flag, hk_s);
 }
 
 size_t simt_smem_bytes(int mode, const DecodeArgs& a) {
@@ -199,7 +204,9 @@ size_t simt_smem_bytes(int mode, const DecodeArgs& a) {
   const int qw = (mode == kRope) ? a.dh : a.rk;
   size_t f = (size_t)a.s * qw + (size_t)TT * a.rk + (size_t)TT * a.rv + (size_t)TT * a.s + 24;
   if (mode == kRope) f += (size_t)TT * a.s * a.dh;
-  return f * sizeof(float);
+  // the split merge reuses everything after the query block as scratch
+  const size_t merge = (size_t)a.s * qw + (size_t)a.s * (a.n_splits + 2) + 16;
+  return (f > merge ? f : merge) * sizeof(float);
 }
 
 template <int MODE, typename KT, typename VT, typename BT>

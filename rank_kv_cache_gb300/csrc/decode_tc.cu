@@ -32,6 +32,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "split_merge.cuh"
 #include "tc_ptx.cuh"
 
 namespace palu {
@@ -87,6 +88,7 @@ constexpr int kSmemAlloc = kSmemBytes + 1024;
 constexpr int kOffO = kOffV;                                // float [2 wg][4][kHeads][kVHalf], reuses the H_v ring
 static_assert(2 * 4 * kHeads * kVHalf * 4 <= kVSlots * kVSlot, "output reduction fits the H_v ring");
 static_assert(kSmemAlloc <= 232448, "shared memory budget");
+static_assert(kHeads * (256 + 2) * 4 <= kVSlots * kVSlot, "split-merge scratch fits the H_v ring");
 
 struct TcParams {
   DecodeArgs a;
@@ -539,6 +541,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::tc_fence_after();
   if (threadIdx.x == 0 && *abort_flag) record_error(a.err, kCodeTimeout, kErrWait, blockIdx.x, b);
   if (warp == 1) tc::tmem_dealloc(tmem_base, kTmemCols);
+  merge_if_last(a, b, head0, kHeads, reinterpret_cast<volatile int*>(smem + kOffMisc + 8),
+                reinterpret_cast<float*>(smem + kOffV));  // the H_v ring is free by now
 }
 
 // ---------------------------------------------------------------------------- host side

@@ -42,6 +42,12 @@ struct DecodeArgs {
   int n_splits;
   int tiles_per_split;
   ErrWord* err;
+  // In-kernel split merge: when `counters` is set, the last CTA of each unit (counted with
+  // an atomic that it resets afterwards) merges that unit's partials into out / lse, and no
+  // merge kernel is launched. counters: [max_batch][n_heads], zero between calls.
+  unsigned* counters;
+  float* out;
+  float* lse;
 };
 
 // create-time set-up
@@ -54,9 +60,11 @@ cudaError_t launch_qprep(int mode, const void* q, int q_dtype, const DecodeArgs&
                          float qscale, float* qbuf, cudaStream_t st);
 cudaError_t launch_decode_simt(int mode, const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_combine(const DecodeArgs& a, float* out, float* lse, cudaStream_t st);
-cudaError_t launch_append(void* cache, __half* scale, int cache_dtype, int64_t capacity, int n_g, int rank,
-                          const void* src, int src_dtype, const int32_t* dst_slot, int batch, int n_new,
-                          ErrWord* err, cudaStream_t st);
+// append the new tokens' key and value latents in one launch
+cudaError_t launch_append(void* cache_k, __half* scale_k, int rank_k, const void* src_k, void* cache_v,
+                          __half* scale_v, int rank_v, const void* src_v, int cache_dtype, int64_t capacity, int n_g,
+                          int src_dtype, const int32_t* dst_slot, int batch, int n_new, ErrWord* err,
+                          cudaStream_t st);
 cudaError_t launch_debug_dequant(const void* cache, const __half* scale, int cache_dtype, int64_t capacity,
                                  int n_g, int rank, int batch, int64_t n_tokens, float* out, cudaStream_t st);
 

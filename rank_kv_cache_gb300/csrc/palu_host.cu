@@ -18,7 +18,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 int elem_bytes(palu_dtype_t t) { return t == PALU_F32 ? 4 : 2; }
 
 struct WsLayout {
-  size_t err, bk, bkt, rope, phase, qbuf, part_o, part_ml, total;
+  size_t err, bk, bkt, rope, phase, qbuf, part_o, part_ml, counters, total;
   int max_splits;
   int64_t max_pos;
 };
@@ -72,6 +72,8 @@ WsLayout layout_of(const palu_attn_desc& d) {
   off = align256(off + (size_t)d.max_batch * d.n_heads * L.max_splits * d.rank_v * sizeof(float));
   L.part_ml = off;
   off = align256(off + (size_t)d.max_batch * d.n_heads * L.max_splits * sizeof(float2));
+  L.counters = off;
+  off = align256(off + (size_t)d.max_batch * d.n_heads * sizeof(unsigned));
   L.total = off;
   return L;
 }
@@ -180,6 +182,8 @@ palu_status_t palu_attn_create(const palu_attn_desc* desc, const void* B_k, void
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(h->ws + L.err, 0, 256, s);
+  if (e == cudaSuccess)
+    e = cudaMemsetAsync(h->ws + L.counters, 0, (size_t)desc->max_batch * desc->n_heads * sizeof(unsigned), s);
   const int cols = desc->group_size * desc->head_dim;
   void* bkt = (desc->mode == PALU_MODE_ROPE && desc->k_dtype != PALU_F32) ? h->ws + L.bkt : nullptr;
   if (e == cudaSuccess)
@@ -286,12 +290,10 @@ palu_status_t palu_append_latents(palu_attn_t h, const palu_cache* cache, const 
   if (cudaSetDevice(h->device) != cudaSuccess) return PALU_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   ErrWord* err = reinterpret_cast<ErrWord*>(h->ws + h->L.err);
-  cudaError_t e = launch_append(cache->hk, static_cast<__half*>(cache->k_scale), to_dt(h->d.k_dtype),
-                                cache->capacity, h->n_g, h->d.rank_k, hk_new, to_dt(src_dtype), dst_slot, batch,
-                                n_new, err, s);
-  if (e == cudaSuccess)
-    e = launch_append(cache->hv, static_cast<__half*>(cache->v_scale), to_dt(h->d.v_dtype), cache->capacity,
-                      h->n_g, h->d.rank_v, hv_new, to_dt(src_dtype), dst_slot, batch, n_new, err, s);
+  const cudaError_t e = launch_append(cache->hk, static_cast<__half*>(cache->k_scale), h->d.rank_k, hk_new,
+                                      cache->hv, static_cast<__half*>(cache->v_scale), h->d.rank_v, hv_new,
+                                      to_dt(h->d.k_dtype), cache->capacity, h->n_g, to_dt(src_dtype), dst_slot, batch,
+                                      n_new, err, s);
   return e == cudaSuccess ? PALU_OK : PALU_ERR_CUDA;
 }
 
@@ -343,6 +345,9 @@ palu_status_t palu_decode_attn(palu_attn_t h, const void* q, const palu_cache* c
   a.part_o = reinterpret_cast<float*>(h->ws + h->L.part_o);
   a.part_ml = reinterpret_cast<float2*>(h->ws + h->L.part_ml);
   a.err = reinterpret_cast<ErrWord*>(h->ws + h->L.err);
+  a.counters = reinterpret_cast<unsigned*>(h->ws + h->L.counters);  // the decode kernels merge the splits
+  a.out = out;
+  a.lse = lse;
 
   const int mode = d.mode == PALU_MODE_ROPE ? kRope : kAbsorbed;
   // kernel choice: tensor-core rebuild (RoPE, fp16/bf16), TMA stream (absorbed, fp16/bf16),
@@ -363,7 +368,6 @@ palu_status_t palu_decode_attn(palu_attn_t h, const void* q, const palu_cache* c
   if (e == cudaSuccess)
     e = use_tc ? launch_decode_tc(a, s) : use_abs ? launch_decode_abs(a, s) : launch_decode_simt(mode, a, s);
   if (tr && e == cudaSuccess) e = cudaEventRecord(tr[1], s);
-  if (e == cudaSuccess) e = launch_combine(a, out, lse, s);
   return e == cudaSuccess ? PALU_OK : PALU_ERR_CUDA;
 }
 

@@ -189,14 +189,16 @@ cudaError_t launch_combine(const DecodeArgs& a, float* out, float* lse, cudaStre
 // code = clamp(rint_half_even(h / scale), -7, 7), 0 when the scale is 0; element 2j in the low
 // nibble of byte j, 2j+1 in the high nibble.
 // ---------------------------------------------------------------------------
-__global__ void append_kernel(void* cache, __half* scale, int cache_dtype, int64_t capacity, int n_g, int rank,
-                              const void* src, int src_dtype, const int32_t* dst_slot, int batch, int n_new,
-                              ErrWord* err) {
-  const int warps = blockDim.x / 32;
-  const int64_t row = (int64_t)blockIdx.x * warps + threadIdx.x / 32;
-  const int lane = threadIdx.x & 31;
-  const int64_t rows = (int64_t)batch * n_new * n_g;
-  if (row >= rows) return;
+struct AppendSide {
+  void* cache;
+  __half* scale;
+  const void* src;
+  int rank;
+};
+
+__device__ void append_row(const AppendSide& sd, int cache_dtype, int64_t capacity, int n_g, int src_dtype,
+                           const int32_t* dst_slot, int n_new, int64_t row, int lane, ErrWord* err) {
+  const int rank = sd.rank;
   const int g = int(row % n_g);
   const int i = int((row / n_g) % n_new);
   const int b = int(row / ((int64_t)n_g * n_new));
@@ -209,11 +211,11 @@ __global__ void append_kernel(void* cache, __half* scale, int cache_dtype, int64
   const int64_t crow = ((int64_t)b * capacity + dst) * n_g + g;
   if (cache_dtype != kINT4) {
     for (int e = lane; e < rank; e += 32) {
-      const float v = load_as_f32(src, src_dtype, src_off + e);
+      const float v = load_as_f32(sd.src, src_dtype, src_off + e);
       const int64_t o = crow * rank + e;
-      if (cache_dtype == kF32) static_cast<float*>(cache)[o] = v;
-      else if (cache_dtype == kF16) static_cast<__half*>(cache)[o] = __float2half_rn(v);
-      else static_cast<__nv_bfloat16*>(cache)[o] = __float2bfloat16_rn(v);
+      if (cache_dtype == kF32) static_cast<float*>(sd.cache)[o] = v;
+      else if (cache_dtype == kF16) static_cast<__half*>(sd.cache)[o] = __float2half_rn(v);
+      else static_cast<__nv_bfloat16*>(sd.cache)[o] = __float2bfloat16_rn(v);
     }
     return;
   }
@@ -224,14 +226,14 @@ __global__ void append_kernel(void* cache, __half* scale, int cache_dtype, int64
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     if (k < per) {
-      h[k] = load_as_f32(src, src_dtype, src_off + lane * per + k);
+      h[k] = load_as_f32(sd.src, src_dtype, src_off + lane * per + k);
       amax = fmaxf(amax, fabsf(h[k]));
     }
   }
   amax = warp_max(amax);
   const __half sc = __float2half_rn(fminf(__fdiv_rn(amax, 7.0f), 65504.0f));
   const float sf = __half2float(sc);
-  uint8_t* out = static_cast<uint8_t*>(cache) + crow * (rank / 2) + lane * (per / 2);
+  uint8_t* out = static_cast<uint8_t*>(sd.cache) + crow * (rank / 2) + lane * (per / 2);
 #pragma unroll
   for (int k = 0; k < 8; k += 2) {
     if (k < per) {
@@ -243,18 +245,33 @@ __global__ void append_kernel(void* cache, __half* scale, int cache_dtype, int64
       out[k / 2] = uint8_t((c0 & 0xF) | ((c1 & 0xF) << 4));
     }
   }
-  if (lane == 0) scale[crow] = sc;
+  if (lane == 0) sd.scale[crow] = sc;
 }
 
-cudaError_t launch_append(void* cache, __half* scale, int cache_dtype, int64_t capacity, int n_g, int rank,
-                          const void* src, int src_dtype, const int32_t* dst_slot, int batch, int n_new,
-                          ErrWord* err, cudaStream_t st) {
+// One warp per (side, b, new token, group) row; rows of the key cache come first, then the
+// value cache, so both are written by one launch.
+__global__ void append_kernel(AppendSide k_side, AppendSide v_side, int cache_dtype, int64_t capacity, int n_g,
+                              int src_dtype, const int32_t* dst_slot, int batch, int n_new, ErrWord* err) {
+  const int warps = blockDim.x / 32;
+  const int64_t gw = (int64_t)blockIdx.x * warps + threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  const int64_t rows = (int64_t)batch * n_new * n_g;
+  if (gw >= 2 * rows) return;
+  if (gw < rows) append_row(k_side, cache_dtype, capacity, n_g, src_dtype, dst_slot, n_new, gw, lane, err);
+  else append_row(v_side, cache_dtype, capacity, n_g, src_dtype, dst_slot, n_new, gw - rows, lane, err);
+}
+
+cudaError_t launch_append(void* cache_k, __half* scale_k, int rank_k, const void* src_k, void* cache_v,
+                          __half* scale_v, int rank_v, const void* src_v, int cache_dtype, int64_t capacity, int n_g,
+                          int src_dtype, const int32_t* dst_slot, int batch, int n_new, ErrWord* err,
+                          cudaStream_t st) {
   const int64_t rows = (int64_t)batch * n_new * n_g;
   if (rows == 0) return cudaSuccess;
   const int warps = 8;
-  const int64_t blocks = (rows + warps - 1) / warps;
-  append_kernel<<<(unsigned)blocks, warps * 32, 0, st>>>(cache, scale, cache_dtype, capacity, n_g, rank, src,
-                                                          src_dtype, dst_slot, batch, n_new, err);
+  const int64_t blocks = (2 * rows + warps - 1) / warps;
+  append_kernel<<<(unsigned)blocks, warps * 32, 0, st>>>(AppendSide{cache_k, scale_k, src_k, rank_k},
+                                                          AppendSide{cache_v, scale_v, src_v, rank_v}, cache_dtype,
+                                                          capacity, n_g, src_dtype, dst_slot, batch, n_new, err);
   return cudaGetLastError();
 }
 
