@@ -47,48 +47,56 @@ constexpr int kN = kHeads * kDh;                 // MMA N
 constexpr int kRank = 256;                       // r_k = r_v (MMA K)
 constexpr int kKChunk = 64;                      // K elements per 128-byte swizzled row
 constexpr int kChunks = kRank / kKChunk;         // 4
-constexpr int kStages = 3;                       // H_k ring
-constexpr int kAStage = kTile * kKChunk * 2;     // 16 KB
+constexpr int kAStage = kTile * kKChunk * 2;     // 16 KB fp16 operand chunk
 constexpr int kBChunk = kN * kKChunk * 2;        // 32 KB
 constexpr int kBBytes = kBChunk * kChunks;       // 128 KB
-constexpr int kVTok = 16;                        // tokens per H_v chunk
-constexpr int kVChunks = kTile / kVTok;          // 8 per tile
-constexpr int kVSlots = 5;                       // H_v ring
-constexpr int kVSlot = kVTok * kRank * 2;        // 8 KB
 constexpr int kVHalf = kRank / 2;                // value columns per softmax/PV warpgroup
 constexpr int kWg = 128;                         // threads per warpgroup
-// Warpgroups: 0 = warp 0 H_k/B producer, warp 1 MMA issuer, warp 2 H_v producer, warp 3 idle;
-// 1, 2 = score warpgroups (rotation pairs 0-31 / 32-63); 3, 4 = softmax/PV warpgroups
-// (value columns 0-127 / 128-255).
-constexpr int kThreads = 5 * kWg;
-// Registers per thread after setmaxnreg; 128*48 + 256*152 + 256*64 = 61440 = 640 threads x
-// the 96 registers each thread is launched with (launch bounds 640 threads, one CTA per SM).
-constexpr int kRegsCtl = 48, kRegsScore = 152, kRegsPv = 64;
-static_assert(kWg * kRegsCtl + 2 * kWg * kRegsScore + 2 * kWg * kRegsPv <= kThreads * 96, "register split");
 constexpr uint32_t kTmemCols = 512;              // two N=256 fp32 accumulators
 constexpr uint64_t kWaitNs = 1000000000ull;      // 1 s per wait
 constexpr float kTurnToRad = 1.4629180792671596e-09f;  // 2 pi / 2^32
 
-// shared-memory map (offsets from a 1024-byte aligned base)
-constexpr int kOffB = 0;
-constexpr int kOffA = kOffB + kBBytes;
-constexpr int kOffV = kOffA + kStages * kAStage;
-constexpr int kOffBar = kOffV + kVSlots * kVSlot;
-// barriers: fullA[3], emptyA[3], bfull[4], tfull[2], tempty[2], vfull[5], vempty[5], sready[2], sfree[2], mma_done
-constexpr int kNumBars = 2 * kStages + kChunks + 2 + 2 + 2 * kVSlots + 2 + 2 + 1;
-constexpr int kOffMisc = kOffBar + 8 * kNumBars;
-constexpr int kOffQ = (kOffMisc + 16 + 15) & ~15;           // float4 [kHalf]: (qa0, qa1, qb0, qb1)
-constexpr int kOffF = kOffQ + kHalf * 16;                   // uint64 [kHalf]
-constexpr int kOffS = kOffF + kHalf * 8;                    // float2 [2 buf][2 part][kTile] partial scores
-constexpr int kOffRed = kOffS + 4 * kTile * 8;              // float2 [2 wg][4]
-constexpr int kOffP = kOffRed + 2 * 4 * 8;                  // float2 [2 wg][kTile]
-constexpr int kOffL = kOffP + 2 * kTile * 8;                // float2 [2 wg][4]
-constexpr int kSmemBytes = kOffL + 2 * 4 * 8;
-constexpr int kSmemAlloc = kSmemBytes + 1024;
-constexpr int kOffO = kOffV;                                // float [2 wg][4][kHeads][kVHalf], reuses the H_v ring
-static_assert(2 * 4 * kHeads * kVHalf * 4 <= kVSlots * kVSlot, "output reduction fits the H_v ring");
-static_assert(kSmemAlloc <= 232448, "shared memory budget");
-static_assert(kHeads * (256 + 2) * 4 <= kVSlots * kVSlot, "split-merge scratch fits the H_v ring");
+// Per-variant layout. I4 = int4 latents: the H_k tile arrives packed (16 KB) and a converter
+// warpgroup expands it into the fp16 operand ring; H_v chunks hold packed rows.
+// Warpgroups: 0 = warp 0 H_k/B producer, warp 1 MMA issuer, warp 2 H_v producer, warp 3 idle;
+// 1, 2 = score warpgroups (rotation pairs 0-31 / 32-63); 3, 4 = softmax/PV warpgroups
+// (value columns 0-127 / 128-255); 5 = int4 converter (I4 only).
+template <bool I4>
+struct Lay {
+  static constexpr int kThreads = (I4 ? 6 : 5) * kWg;
+  static constexpr int kLaunchRegs = I4 ? 80 : 96;  // per thread at launch (launch bounds, one CTA per SM)
+  static constexpr int kRegsCtl = I4 ? 40 : 48, kRegsScore = I4 ? 128 : 152, kRegsPv = 64, kRegsConv = 48;
+  static constexpr int kStages = I4 ? 2 : 3;        // fp16 H_k operand ring
+  static constexpr int kPStages = I4 ? 2 : 0;       // packed int4 H_k tiles
+  static constexpr int kPStage = kTile * (kRank / 2);
+  static constexpr int kVTok = I4 ? 64 : 16;        // tokens per H_v chunk
+  static constexpr int kVRow = I4 ? kRank / 2 : kRank * 2;
+  static constexpr int kVSlot = kVTok * kVRow;      // 8 KB
+  static constexpr int kVSlots = I4 ? 2 : 5;
+  static constexpr int kVChunks = kTile / kVTok;
+  static constexpr int kOffB = 0;
+  static constexpr int kOffA = kOffB + kBBytes;
+  static constexpr int kOffPk = kOffA + kStages * kAStage;
+  static constexpr int kOffV = kOffPk + kPStages * kPStage;
+  static constexpr int kOffBar = kOffV + kVSlots * kVSlot;
+  static constexpr int kNumBars = 48;
+  static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
+  static constexpr int kOffQ = (kOffMisc + 16 + 15) & ~15;     // float4 [kHalf]: (qa0, qa1, qb0, qb1)
+  static constexpr int kOffF = kOffQ + kHalf * 16;             // uint64 [kHalf]
+  static constexpr int kOffS = kOffF + kHalf * 8;              // float2 [2 buf][2 part][kTile]
+  static constexpr int kOffRed = kOffS + 4 * kTile * 8;        // float2 [2 wg][4]
+  static constexpr int kOffP = kOffRed + 2 * 4 * 8;            // float2 [2 wg][kTile]
+  static constexpr int kOffL = kOffP + 2 * kTile * 8;          // float2 [2 wg][4]
+  static constexpr int kSmemBytes = kOffL + 2 * 4 * 8;
+  static constexpr int kSmemAlloc = kSmemBytes + 1024;
+  static constexpr int kOffO = kOffV;                          // [2 wg][4][kHeads][kVHalf] floats
+  static_assert(kWg * kRegsCtl + 2 * kWg * kRegsScore + 2 * kWg * kRegsPv + (I4 ? kWg * kRegsConv : 0) <=
+                    kThreads * kLaunchRegs,
+                "register split");
+  static_assert(2 * 4 * kHeads * kVHalf * 4 <= kVSlots * kVSlot, "output reduction fits the H_v ring");
+  static_assert(kHeads * (256 + 2) * 4 <= kVSlots * kVSlot, "split-merge scratch fits the H_v ring");
+  static_assert(kSmemAlloc <= 232448, "shared memory budget");
+};
 
 struct TcParams {
   DecodeArgs a;
@@ -114,6 +122,32 @@ __device__ __forceinline__ void unpack4<__nv_bfloat16>(const uint2& u, float* h)
   h[2] = __uint_as_float(u.y << 16);
   h[3] = __uint_as_float(u.y & 0xffff0000u);
 }
+// four signed 4-bit codes (element order: low nibble first) as floats
+__device__ __forceinline__ void unpack4_int4(uint32_t two_bytes, float* h) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = float(int32_t(two_bytes << (28 - 4 * i)) >> 28);
+}
+// eight signed 4-bit codes of a 32-bit word (element 2j = low nibble of byte j) as eight
+// exact fp16 values: each nibble biased by 8 is placed under the fp16 exponent of 1024
+// (0x64xx), and 1032 is subtracted.
+__device__ __forceinline__ uint4 int4x8_to_half8(uint32_t w) {
+  const uint32_t lo = (w & 0x0F0F0F0Fu) ^ 0x08080808u;
+  const uint32_t hi = ((w >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
+  const uint32_t i01 = __byte_perm(lo, hi, 0x5140);   // lo0 hi0 lo1 hi1
+  const uint32_t i23 = __byte_perm(lo, hi, 0x7362);   // lo2 hi2 lo3 hi3
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));  // 1032
+  uint32_t r[4];
+  r[0] = __byte_perm(i01, 0x64646464u, 0x4140);
+  r[1] = __byte_perm(i01, 0x64646464u, 0x4342);
+  r[2] = __byte_perm(i23, 0x64646464u, 0x4140);
+  r[3] = __byte_perm(i23, 0x64646464u, 0x4342);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&r[i]), bias);
+    r[i] = *reinterpret_cast<const uint32_t*>(&v);
+  }
+  return make_uint4(r[0], r[1], r[2], r[3]);
+}
 
 __device__ __forceinline__ int token_position(const DecodeArgs& a, int b, int t, bool valid) {
   int pos = t;
@@ -134,10 +168,14 @@ __device__ __forceinline__ void setmaxnreg_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
-template <typename VT>
-__global__ void __launch_bounds__(kThreads, 1)
+// VT = value-latent storage (__half, __nv_bfloat16, or Int4); I4 = int4 latents (fp16 MMA operands)
+template <typename VT, bool I4>
+__global__ void __launch_bounds__(Lay<I4>::kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_hk, const __grid_constant__ CUtensorMap tm_hv,
                      const __grid_constant__ CUtensorMap tm_b, const TcParams P) {
+  using LY = Lay<I4>;
+  constexpr int kStages = LY::kStages, kPStages = LY::kPStages, kVSlots = LY::kVSlots, kVTok = LY::kVTok;
+  constexpr int kVChunks = LY::kVChunks, kVSlot = LY::kVSlot, kVRow = LY::kVRow;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const DecodeArgs& a = P.a;
@@ -146,22 +184,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int hp = blockIdx.x % P.hp_count, split = blockIdx.x / P.hp_count;
   const int g = blockIdx.y, b = blockIdx.z;
 
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint64_t* fullA = bars;
-  uint64_t* emptyA = fullA + kStages;
-  uint64_t* bfull = emptyA + kStages;
-  uint64_t* tfull = bfull + kChunks;
-  uint64_t* tempty = tfull + 2;
-  uint64_t* vfull = tempty + 2;
-  uint64_t* vempty = vfull + kVSlots;
-  uint64_t* sready = vempty + kVSlots;
-  uint64_t* sfree = sready + 2;
-  uint64_t* mma_done = sfree + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
-  float4* qs = reinterpret_cast<float4*>(smem + kOffQ);
-  uint64_t* Fs = reinterpret_cast<uint64_t*>(smem + kOffF);
-  float2* sbuf = reinterpret_cast<float2*>(smem + kOffS);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LY::kOffBar);
+  uint64_t* fullA = bars;                 // [kStages]
+  uint64_t* emptyA = bars + 4;            // [kStages]
+  uint64_t* bfull = bars + 8;             // [kChunks]
+  uint64_t* tfull = bars + 12;            // [2]
+  uint64_t* tempty = bars + 14;           // [2]
+  uint64_t* vfull = bars + 16;            // [kVSlots]
+  uint64_t* vempty = bars + 24;           // [kVSlots]
+  uint64_t* sready = bars + 32;           // [2]
+  uint64_t* sfree = bars + 34;            // [2]
+  uint64_t* pfull = bars + 36;            // [kPStages]
+  uint64_t* pempty = bars + 40;           // [kPStages]
+  uint64_t* mma_done = bars + 44;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + LY::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + LY::kOffMisc + 4);
+  float4* qs = reinterpret_cast<float4*>(smem + LY::kOffQ);
+  uint64_t* Fs = reinterpret_cast<uint64_t*>(smem + LY::kOffF);
+  float2* sbuf = reinterpret_cast<float2*>(smem + LY::kOffS);
 
   // this CTA's token range
   int T = a.seq_lens[b];
@@ -178,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      tc::mbar_init(&fullA[i], 1);
+      tc::mbar_init(&fullA[i], I4 ? 4 : 1);   // converter warps, or the TMA
       tc::mbar_init(&emptyA[i], 1);
     }
     for (int i = 0; i < kChunks; ++i) tc::mbar_init(&bfull[i], 1);
@@ -191,6 +231,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < kVSlots; ++i) {
       tc::mbar_init(&vfull[i], 1);
       tc::mbar_init(&vempty[i], 8);   // eight softmax/PV warps
+    }
+    for (int i = 0; i < kPStages; ++i) {
+      tc::mbar_init(&pfull[i], 1);
+      tc::mbar_init(&pempty[i], 4);   // converter warps
     }
     tc::mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -227,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   if (wg == 0) {
-    setmaxnreg_dec<kRegsCtl>();
+    setmaxnreg_dec<LY::kRegsCtl>();
     if (warp == 0) {
       // ---------------------------------------------------------- H_k / B producer
       if (lane == 0 && n_tiles > 0) {
@@ -236,37 +280,60 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int brow = g * (a.s * kDh) + hp * kN;
         for (int kc = 0; kc < kChunks; ++kc) {
           tc::mbar_arrive_expect_tx(&bfull[kc], kBChunk);
-          tc::tma_load_2d(smem + kOffB + kc * kBChunk, &tm_b, &bfull[kc], kc * kKChunk, brow);
+          tc::tma_load_2d(smem + LY::kOffB + kc * kBChunk, &tm_b, &bfull[kc], kc * kKChunk, brow);
         }
-        int stage = 0, issued = 0;
-        uint32_t round = 0;
         bool ok = true;
-        for (int it = 0; it < n_tiles && ok; ++it) {
-          const int t0 = t_begin + it * kTile;
-          for (int kc = 0; kc < kChunks; ++kc) {
-            if (!tc::mbar_wait_bounded(&emptyA[stage], (round & 1) ^ 1, abort_flag, kWaitNs)) {
+        int issued = 0;
+        if constexpr (I4) {
+          // whole packed tiles (128 tokens x 128 bytes) into the staging ring
+          for (int it = 0; it < n_tiles && ok; ++it) {
+            const int ps = it % kPStages;
+            if (!tc::mbar_wait_bounded(&pempty[ps], ((it / kPStages) & 1) ^ 1, abort_flag, kWaitNs)) {
               ok = false;
               break;
             }
-            tc::mbar_arrive_expect_tx(&fullA[stage], kAStage);
-            tc::tma_load_3d(smem + kOffA + stage * kAStage, &tm_hk, &fullA[stage], kc * kKChunk, g, row0 + t0);
+            tc::mbar_arrive_expect_tx(&pfull[ps], LY::kPStage);
+            tc::tma_load_3d(smem + LY::kOffPk + ps * LY::kPStage, &tm_hk, &pfull[ps], 0, g, row0 + t_begin + it * kTile);
             ++issued;
-            if (++stage == kStages) {
-              stage = 0;
-              ++round;
+          }
+          if (!ok) {
+            volatile int quiet = 0;
+            for (int it = (issued > kPStages ? issued - kPStages : 0); it < issued; ++it)
+              tc::mbar_wait_bounded(&pfull[it % kPStages], (it / kPStages) & 1, &quiet, kWaitNs / 10);
+          }
+        } else {
+          int stage = 0;
+          uint32_t round = 0;
+          for (int it = 0; it < n_tiles && ok; ++it) {
+            const int t0 = t_begin + it * kTile;
+            for (int kc = 0; kc < kChunks; ++kc) {
+              if (!tc::mbar_wait_bounded(&emptyA[stage], (round & 1) ^ 1, abort_flag, kWaitNs)) {
+                ok = false;
+                break;
+              }
+              tc::mbar_arrive_expect_tx(&fullA[stage], kAStage);
+              tc::tma_load_3d(smem + LY::kOffA + stage * kAStage, &tm_hk, &fullA[stage], kc * kKChunk, g, row0 + t0);
+              ++issued;
+              if (++stage == kStages) {
+                stage = 0;
+                ++round;
+              }
+            }
+          }
+          if (!ok) {
+            // drain the copies still in flight before the CTA may exit
+            volatile int quiet = 0;
+            for (int k = 0, s = stage, r = (int)round; k < (issued < kStages ? issued : kStages); ++k) {
+              if (--s < 0) {
+                s = kStages - 1;
+                --r;
+              }
+              tc::mbar_wait_bounded(&fullA[s], uint32_t(r) & 1, &quiet, kWaitNs / 10);
             }
           }
         }
         if (!ok) {
-          // drain the copies still in flight before the CTA may exit
           volatile int quiet = 0;
-          for (int k = 0, s = stage, r = (int)round; k < (issued < kStages ? issued : kStages); ++k) {
-            if (--s < 0) {
-              s = kStages - 1;
-              --r;
-            }
-            tc::mbar_wait_bounded(&fullA[s], uint32_t(r) & 1, &quiet, kWaitNs / 10);
-          }
           for (int kc = 0; kc < kChunks; ++kc) tc::mbar_wait_bounded(&bfull[kc], 0, &quiet, kWaitNs / 10);
         }
       }
@@ -277,8 +344,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         int stage = 0;
         uint32_t round = 0;
-        const uint32_t a_base = tc::smem_addr(smem + kOffA);
-        const uint32_t b_base = tc::smem_addr(smem + kOffB);
+        const uint32_t a_base = tc::smem_addr(smem + LY::kOffA);
+        const uint32_t b_base = tc::smem_addr(smem + LY::kOffB);
         for (int it = 0; it < n_tiles && ok; ++it) {
           const int buf = it & 1;
           const uint32_t use = it >> 1;
@@ -334,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             tc::mbar_arrive_expect_tx(&vfull[slot], kVSlot);
-            tc::tma_load_3d(smem + kOffV + slot * kVSlot, &tm_hv, &vfull[slot], 0, g, row0 + t0 + ch * kVTok);
+            tc::tma_load_3d(smem + LY::kOffV + slot * kVSlot, &tm_hv, &vfull[slot], 0, g, row0 + t0 + ch * kVTok);
             ++issued;
           }
         }
@@ -349,19 +416,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ score warpgroups
     // thread = one token row of the tile; warpgroup X handles rotation pairs 32X..32X+31 of
     // both heads: rotate each rebuilt key pair at the token's position, dot it with the
-    // rotated query, and leave the partial scores in shared memory.
-    setmaxnreg_inc<kRegsScore>();
+    // rotated query, and leave the partial scores in shared memory. For int4 latents the MMA
+    // ran on the integer codes and the token's key scale multiplies the score (RoPE and the
+    // dot product are linear in the key).
+    setmaxnreg_inc<LY::kRegsScore>();
     const int X = wg - 1;
     const int quad = warp & 3;               // TMEM lane quadrant this warp may access
     const int row = quad * 32 + lane;
     int pos_next = token_position(a, b, t_begin + row, t_begin + row < t_end);
+    float ks_next = 1.f;
+    if constexpr (I4)
+      if (t_begin + row < t_end) ks_next = __half2float(a.k_scale[((int64_t)row0 + t_begin + row) * a.n_g + g]);
     for (int it = 0; it < n_tiles; ++it) {
       const int buf = it & 1;
       const uint32_t use = it >> 1;
       const int t0 = t_begin + it * kTile;
       const bool valid = t0 + row < t_end;
       const uint32_t upos = uint32_t(pos_next);
-      if (it + 1 < n_tiles) pos_next = token_position(a, b, t0 + kTile + row, t0 + kTile + row < t_end);
+      const float ks = ks_next;
+      if (it + 1 < n_tiles) {
+        const int tn = t0 + kTile + row;
+        pos_next = token_position(a, b, tn, tn < t_end);
+        if constexpr (I4)
+          if (tn < t_end) ks_next = __half2float(a.k_scale[((int64_t)row0 + tn) * a.n_g + g]);
+      }
 
       const bool got = tc::mbar_wait_bounded(&tfull[buf], use & 1, abort_flag, kWaitNs) &&
                        tc::mbar_wait_bounded(&sfree[buf], (use & 1) ^ 1, abort_flag, kWaitNs);
@@ -405,23 +483,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&tempty[buf]);
       sbuf[(buf * 2 + X) * kTile + row] =
-          valid ? make_float2(s0a + s0b, s1a + s1b) : make_float2(-INFINITY, -INFINITY);
+          valid ? make_float2((s0a + s0b) * ks, (s1a + s1b) * ks) : make_float2(-INFINITY, -INFINITY);
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&sready[buf]);
     }
-  } else {
+  } else if (wg <= 4) {
     // ------------------------------------------------------------ softmax / PV warpgroups
     // Both warpgroups run the same online softmax over the tile's 128 scores (summing the two
-    // partial scores); warpgroup Y accumulates p H_v for value columns 128Y..128Y+127.
-    setmaxnreg_dec<kRegsPv>();
+    // partial scores); warpgroup Y accumulates p H_v for value columns 128Y..128Y+127. For
+    // int4 latents p is multiplied by the token's value scale before it weights the codes.
+    setmaxnreg_dec<LY::kRegsPv>();
     const int Y = wg - 3;
     const int e = warp & 3;                  // warp within the warpgroup
     const int ei = threadIdx.x - wg * kWg;   // 0..127: token row for the softmax
     const int bar = 3 + Y;
-    float2* red = reinterpret_cast<float2*>(smem + kOffRed) + Y * 4;
-    float2* pbuf = reinterpret_cast<float2*>(smem + kOffP) + Y * kTile;
-    float2* lred = reinterpret_cast<float2*>(smem + kOffL) + Y * 4;
-    float* ored = reinterpret_cast<float*>(smem + kOffO) + Y * (4 * kHeads * kVHalf);
+    float2* red = reinterpret_cast<float2*>(smem + LY::kOffRed) + Y * 4;
+    float2* pbuf = reinterpret_cast<float2*>(smem + LY::kOffP) + Y * kTile;
+    float2* lred = reinterpret_cast<float2*>(smem + LY::kOffL) + Y * 4;
+    float* ored = reinterpret_cast<float*>(smem + LY::kOffO) + Y * (4 * kHeads * kVHalf);
     float m_run0 = -INFINITY, m_run1 = -INFINITY;
     float l0 = 0.f, l1 = 0.f;
     float acc0[4], acc1[4];
@@ -429,11 +508,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int c = 0; c < 4; ++c) acc0[c] = acc1[c] = 0.f;
     bool aborted = false;  // warpgroup-uniform: only ever set from a barrier-OR
     bool broken = false;   // this warp's own H_v wait gave up
+    float vs_next = 1.f;
+    if constexpr (I4)
+      if (t_begin + ei < t_end) vs_next = __half2float(a.v_scale[((int64_t)row0 + t_begin + ei) * a.n_g + g]);
 
     for (int it = 0; it < n_tiles; ++it) {
       const int buf = it & 1;
       const uint32_t use = it >> 1;
       const int t0 = t_begin + it * kTile;
+      const float vsc = vs_next;
+      if constexpr (I4)
+        if (it + 1 < n_tiles && t0 + kTile + ei < t_end)
+          vs_next = __half2float(a.v_scale[((int64_t)row0 + t0 + kTile + ei) * a.n_g + g]);
       const bool got = tc::mbar_wait_bounded(&sready[buf], use & 1, abort_flag, kWaitNs);
       if (tc::named_bar_or(bar, kWg, !got || broken)) {
         aborted = true;
@@ -464,44 +550,76 @@ __global__ void __launch_bounds__(kThreads, 1)
       m_run1 = mn1;
       l0 = l0 * al0 + p0;
       l1 = l1 * al1 + p1;
-      pbuf[ei] = make_float2(p0, p1);
+      pbuf[ei] = I4 ? make_float2(p0 * vsc, p1 * vsc) : make_float2(p0, p1);
       tc::named_bar(bar, kWg);
 
-      // p H_v over 16-token chunks; warp e takes 4 tokens of each chunk and lane owns
-      // columns 128Y + 4 lane .. 128Y + 4 lane + 3. A warp whose wait gave up skips the
-      // arithmetic; the tile-level barrier-OR above then ends the loop for the warpgroup.
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         acc0[c] *= al0;
         acc1[c] *= al1;
       }
-      for (int ch = 0; ch < kVChunks; ch += 2) {
-        uint2 u[8];
-#pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {
-          const int vi = it * kVChunks + ch + c2;
+      if constexpr (I4) {
+        // p H_v over 64-token chunks of packed rows; warp e takes 16 tokens of each chunk and
+        // lane owns the codes of columns 128Y + 4 lane .. 128Y + 4 lane + 3 (two bytes)
+        for (int ch = 0; ch < kVChunks; ++ch) {
+          const int vi = it * kVChunks + ch;
           const int slot = vi % kVSlots;
           if (!tc::mbar_wait_bounded(&vfull[slot], (vi / kVSlots) & 1, abort_flag, kWaitNs)) broken = true;
-          const uint8_t* vs = smem + kOffV + slot * kVSlot + (e * 4) * (kRank * 2) + (Y * kVHalf + lane * 4) * 2;
+          const uint8_t* vs = smem + LY::kOffV + slot * kVSlot + (e * 16) * kVRow + Y * (kVHalf / 2) + lane * 2;
+          uint32_t u[16];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) u[c2 * 4 + k] = *reinterpret_cast<const uint2*>(vs + k * (kRank * 2));
+          for (int k = 0; k < 16; ++k) u[k] = *reinterpret_cast<const uint16_t*>(vs + k * kVRow);
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(&vempty[slot]);
+          if (broken) continue;
+          const bool all = t0 + ch * kVTok + e * 16 + 15 < t_end;
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const int tk = ch * kVTok + e * 16 + k;
+            if (all || t0 + tk < t_end) {
+              float h[4];
+              unpack4_int4(u[k], h);
+              const float2 p = pbuf[tk];
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                acc0[c] = fmaf(p.x, h[c], acc0[c]);
+                acc1[c] = fmaf(p.y, h[c], acc1[c]);
+              }
+            }
+          }
         }
-        if (broken) continue;
-        // all eight tokens valid (every tile but the last): no per-token branch
-        const bool all = t0 + (ch + 1) * kVTok + e * 4 + 3 < t_end;
+      } else {
+        // p H_v over 16-token chunks; warp e takes 4 tokens of each chunk and lane owns
+        // columns 128Y + 4 lane .. 128Y + 4 lane + 3. A warp whose wait gave up skips the
+        // arithmetic; the tile-level barrier-OR above then ends the loop for the warpgroup.
+        for (int ch = 0; ch < kVChunks; ch += 2) {
+          uint2 u[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int tk = (ch + (k >> 2)) * kVTok + e * 4 + (k & 3);   // token index within the tile
-          if (all || t0 + tk < t_end) {
-            float h[4];
-            unpack4<VT>(u[k], h);
-            const float2 p = pbuf[tk];
+          for (int c2 = 0; c2 < 2; ++c2) {
+            const int vi = it * kVChunks + ch + c2;
+            const int slot = vi % kVSlots;
+            if (!tc::mbar_wait_bounded(&vfull[slot], (vi / kVSlots) & 1, abort_flag, kWaitNs)) broken = true;
+            const uint8_t* vs = smem + LY::kOffV + slot * kVSlot + (e * 4) * kVRow + (Y * kVHalf + lane * 4) * 2;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              acc0[c] = fmaf(p.x, h[c], acc0[c]);
-              acc1[c] = fmaf(p.y, h[c], acc1[c]);
+            for (int k = 0; k < 4; ++k) u[c2 * 4 + k] = *reinterpret_cast<const uint2*>(vs + k * kVRow);
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&vempty[slot]);
+          }
+          if (broken) continue;
+          // all eight tokens valid (every tile but the last): no per-token branch
+          const bool all = t0 + (ch + 1) * kVTok + e * 4 + 3 < t_end;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int tk = (ch + (k >> 2)) * kVTok + e * 4 + (k & 3);   // token index within the tile
+            if (all || t0 + tk < t_end) {
+              float h[4];
+              unpack4<VT>(u[k], h);
+              const float2 p = pbuf[tk];
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                acc0[c] = fmaf(p.x, h[c], acc0[c]);
+                acc1[c] = fmaf(p.y, h[c], acc1[c]);
+              }
             }
           }
         }
@@ -534,6 +652,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         a.part_ml[bh * a.n_splits + split] = make_float2(ei == 0 ? m_run0 : m_run1, L);
       }
     }
+  } else {
+    // ------------------------------------------------------------ int4 converter (I4 only)
+    // thread = one token row: expand the row's packed codes into exact fp16 codes in the MMA
+    // operand ring (128-byte swizzle, one 64-column chunk per stage).
+    if constexpr (I4) {
+      setmaxnreg_dec<LY::kRegsConv>();
+      const int r = threadIdx.x - 5 * kWg;
+      bool ok = true;
+      for (int it = 0; it < n_tiles && ok; ++it) {
+        const int ps = it % kPStages;
+        if (!tc::mbar_wait_bounded(&pfull[ps], (it / kPStages) & 1, abort_flag, kWaitNs)) break;
+        const uint8_t* prow = smem + LY::kOffPk + ps * LY::kPStage + r * 128;
+        for (int kc = 0; kc < kChunks; ++kc) {
+          const int si = it * kChunks + kc;
+          const int stage = si % kStages;
+          if (!tc::mbar_wait_bounded(&emptyA[stage], ((si / kStages) & 1) ^ 1, abort_flag, kWaitNs)) {
+            ok = false;
+            break;
+          }
+          // packed bytes 32 kc .. 32 kc + 31 of the row = 16-byte chunks 2 kc, 2 kc + 1 (swizzled)
+          const uint4 w0 = *reinterpret_cast<const uint4*>(prow + (((2 * kc) ^ (r & 7)) << 4));
+          const uint4 w1 = *reinterpret_cast<const uint4*>(prow + (((2 * kc + 1) ^ (r & 7)) << 4));
+          const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+          uint8_t* arow = smem + LY::kOffA + stage * kAStage + r * 128;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) *reinterpret_cast<uint4*>(arow + ((j ^ (r & 7)) << 4)) = int4x8_to_half8(wv[j]);
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor cores
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&fullA[stage]);
+        }
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&pempty[ps]);
+      }
+    }
   }
 
   tc::tc_fence_before();
@@ -541,8 +693,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::tc_fence_after();
   if (threadIdx.x == 0 && *abort_flag) record_error(a.err, kCodeTimeout, kErrWait, blockIdx.x, b);
   if (warp == 1) tc::tmem_dealloc(tmem_base, kTmemCols);
-  merge_if_last(a, b, head0, kHeads, reinterpret_cast<volatile int*>(smem + kOffMisc + 8),
-                reinterpret_cast<float*>(smem + kOffV));  // the H_v ring is free by now
+  merge_if_last(a, b, head0, kHeads, reinterpret_cast<volatile int*>(smem + LY::kOffMisc + 8),
+                reinterpret_cast<float*>(smem + LY::kOffV));  // the H_v ring is free by now
 }
 
 // ---------------------------------------------------------------------------- host side
@@ -575,56 +727,70 @@ bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, 
 }  // namespace
 
 bool tc_supported(const DecodeArgs& a) {
-  return (a.k_dtype == kF16 || a.k_dtype == kBF16) && a.v_dtype == a.k_dtype && a.dh == kDh && a.rk == kRank &&
-         a.rv == kRank && a.s % kHeads == 0 && (int64_t)a.batch * a.capacity >= kTile &&
-         (int64_t)a.batch * a.capacity < (int64_t(1) << 31) && encode_fn() != nullptr;
+  const bool i4 = a.k_dtype == kINT4;
+  return (a.k_dtype == kF16 || a.k_dtype == kBF16 || i4) && a.v_dtype == a.k_dtype &&
+         (!i4 || a.bk_dtype == kF16) && a.dh == kDh && a.rk == kRank && a.rv == kRank && a.s % kHeads == 0 &&
+         (int64_t)a.batch * a.capacity >= kTile && (int64_t)a.batch * a.capacity < (int64_t(1) << 31) &&
+         encode_fn() != nullptr;
 }
 
 int tc_tile_tokens() { return kTile; }
 int tc_ctas_per_group(const DecodeArgs& a) { return a.s / kHeads; }
 
+template <typename VT, bool I4>
+cudaError_t launch_variant(const CUtensorMap& tm_hk, const CUtensorMap& tm_hv, const CUtensorMap& tm_b,
+                           const TcParams& P, cudaStream_t st) {
+  auto kern = decode_tc_kernel<VT, I4>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<I4>::kSmemAlloc);
+  if (e != cudaSuccess) return e;
+  dim3 grid(P.a.n_splits * P.hp_count, P.a.n_g, P.a.batch);
+  kern<<<grid, Lay<I4>::kThreads, Lay<I4>::kSmemAlloc, st>>>(tm_hk, tm_hv, tm_b, P);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st) {
   if (!encode_fn()) return cudaErrorNotSupported;
+  const bool i4 = a.k_dtype == kINT4;
   const CUtensorMapDataType dt = a.k_dtype == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUtensorMap tm_hk, tm_hv, tm_b;
   const cuuint64_t rows = (cuuint64_t)a.batch * a.capacity;
-  {
+  if (i4) {
+    // packed rows [rows][n_g][r/2] bytes: H_k as whole 128-token tiles (128-byte swizzle for the
+    // converter's row reads), H_v as 64-token chunks
+    const cuuint64_t dims[3] = {(cuuint64_t)kRank / 2, (cuuint64_t)a.n_g, rows};
+    const cuuint64_t strides[2] = {(cuuint64_t)kRank / 2, (cuuint64_t)a.n_g * (kRank / 2)};
+    const cuuint32_t boxk[3] = {kRank / 2, 1, kTile};
+    const cuuint32_t boxv[3] = {kRank / 2, 1, (cuuint32_t)Lay<true>::kVTok};
+    if (!encode(&tm_hk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, a.hk, dims, strides, boxk, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+    if (!encode(&tm_hv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, a.hv, dims, strides, boxv, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+  } else {
     // H_k as [rows][n_g][r]: boxes of 64 ranks x 1 group x 128 tokens, 128-byte swizzle (MMA operand)
     const cuuint64_t dims[3] = {(cuuint64_t)a.rk, (cuuint64_t)a.n_g, rows};
     const cuuint64_t strides[2] = {(cuuint64_t)a.rk * 2, (cuuint64_t)a.n_g * a.rk * 2};
-    const cuuint32_t box[3] = {kKChunk, 1, kTile};
-    if (!encode(&tm_hk, dt, 3, a.hk, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
-  }
-  {
-    // H_v as [rows][n_g][r]: boxes of whole 512-byte rows x 32 tokens, unswizzled (row reads)
-    const cuuint64_t dims[3] = {(cuuint64_t)a.rv, (cuuint64_t)a.n_g, rows};
-    const cuuint64_t strides[2] = {(cuuint64_t)a.rv * 2, (cuuint64_t)a.n_g * a.rv * 2};
-    const cuuint32_t box[3] = {(cuuint32_t)kRank, 1, kVTok};
-    if (!encode(&tm_hv, dt, 3, a.hv, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE)) return cudaErrorInvalidValue;
+    const cuuint32_t boxk[3] = {kKChunk, 1, kTile};
+    if (!encode(&tm_hk, dt, 3, a.hk, dims, strides, boxk, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+    // H_v: whole 512-byte rows x 16 tokens, unswizzled (row reads)
+    const cuuint32_t boxv[3] = {(cuuint32_t)kRank, 1, (cuuint32_t)Lay<false>::kVTok};
+    if (!encode(&tm_hv, dt, 3, a.hv, dims, strides, boxv, CU_TENSOR_MAP_SWIZZLE_NONE)) return cudaErrorInvalidValue;
   }
   {
     // B_k^T as [n_g * s * d_h][r]: boxes of 64 ranks x 256 rows, 128-byte swizzle
     const cuuint64_t dims[2] = {(cuuint64_t)a.rk, (cuuint64_t)a.n_g * a.s * a.dh};
     const cuuint64_t strides[1] = {(cuuint64_t)a.rk * 2};
     const cuuint32_t box[2] = {kKChunk, kN};
-    if (!encode(&tm_b, dt, 2, a.bkt, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+    if (!encode(&tm_b, i4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : dt, 2, a.bkt, dims, strides, box,
+                CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
   }
   TcParams P;
   P.a = a;
   P.hp_count = a.s / kHeads;
   P.bf16 = a.k_dtype == kBF16;
-  dim3 grid(a.n_splits * P.hp_count, a.n_g, a.batch);
-  cudaError_t e;
-  if (a.k_dtype == kBF16) {
-    e = cudaFuncSetAttribute(decode_tc_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
-    if (e != cudaSuccess) return e;
-    decode_tc_kernel<__nv_bfloat16><<<grid, kThreads, kSmemAlloc, st>>>(tm_hk, tm_hv, tm_b, P);
-  } else {
-    e = cudaFuncSetAttribute(decode_tc_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
-    if (e != cudaSuccess) return e;
-    decode_tc_kernel<__half><<<grid, kThreads, kSmemAlloc, st>>>(tm_hk, tm_hv, tm_b, P);
-  }
-  return cudaGetLastError();
+  if (i4) return launch_variant<Int4, true>(tm_hk, tm_hv, tm_b, P, st);
+  if (a.k_dtype == kBF16) return launch_variant<__nv_bfloat16, false>(tm_hk, tm_hv, tm_b, P, st);
+  return launch_variant<__half, false>(tm_hk, tm_hv, tm_b, P, st);
 }
 
 }  // namespace palu

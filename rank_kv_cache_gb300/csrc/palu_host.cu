@@ -350,8 +350,8 @@ palu_status_t palu_decode_attn(palu_attn_t h, const void* q, const palu_cache* c
   a.lse = lse;
 
   const int mode = d.mode == PALU_MODE_ROPE ? kRope : kAbsorbed;
-  // kernel choice: tensor-core rebuild (RoPE, fp16/bf16), TMA stream (absorbed, fp16/bf16),
-  // CUDA-core kernel for everything else (fp32 and int4 latents, other shapes)
+  // kernel choice: tensor-core rebuild (RoPE; fp16, bf16 and int4 latents), TMA stream (absorbed,
+  // fp16/bf16), CUDA-core kernel for everything else (fp32 latents, int4 absorbed, other shapes)
   const bool use_tc = mode == kRope && tc_supported(a);
   const bool use_abs = mode == kAbsorbed && abs_supported(a);
   const int tile = use_tc ? tc_tile_tokens() : use_abs ? abs_stage_tokens() : kSimtTile;

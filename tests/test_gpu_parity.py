@@ -112,6 +112,28 @@ def test_int4_rope_hadamard_ragged():
     assert_close(out, ref, lse, lse_ref)
 
 
+@pytest.mark.parametrize("T", [64, 127, 128, 129, 1000])
+def test_int4_rope_tile_edges(T):
+    # batch * capacity >= 128: the tensor-core kernel with the int4 converter
+    cfg = gen.CONFIGS[5].with_(T=T, batch=2)
+    c = Case(cfg, seq_lens=[T, max(1, (T * 2) // 3)])
+    out, lse = c.run_gpu()
+    ref, lse_ref = c.run_oracle()
+    assert_close(out, ref, lse, lse_ref)
+
+
+def test_int4_rope_positions_and_split_plan():
+    cfg = gen.CONFIGS[5].with_(T=700, batch=2)
+    rng = np.random.default_rng(11)
+    pos = np.stack([rng.permutation(3000)[:700] for _ in range(2)]).astype(np.int32)
+    c = Case(cfg, seq_lens=[700, 450], positions=pos, q_pos=[2999, 5], capacity=4096, max_position=3000)
+    a, la = c.run_gpu()
+    b, lb = c.run_gpu(max_seq_len=4096)
+    ref, lse_ref = c.run_oracle()
+    assert_close(a, ref, la, lse_ref)
+    assert_close(b, ref, lb, lse_ref)
+
+
 def test_device_error_word_on_bad_position():
     from rank_kv_cache_gb300 import palu as P
     cfg = gen.CONFIGS[2].with_(T=64, batch=1)
