@@ -13,6 +13,7 @@ instead, on a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -97,6 +98,45 @@ def roofline_for(cfg, work, kernel_ms, peaks, peaks_src, long_step):
     ach = work["decode_bytes"] / sec / 1e9
     return {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s", "frac": round(ach / hbm, 4),
             "traffic": None, "peak_source": f"hbm_gbs of {peaks_src}"}
+
+
+# ---------------------------------------------------------------------------
+# DRAM traffic of the decode kernel, from a recorded ncu capture
+# ---------------------------------------------------------------------------
+
+CSRC = os.path.join(ROOT, "rank_kv_cache_gb300", "csrc")
+KERNEL_SOURCES = {
+    "decode_tc_kernel": ("decode_tc.cu", "tc_ptx.cuh"),
+    "decode_abs_kernel": ("decode_abs.cu", "tc_ptx.cuh"),
+    "decode_simt_kernel": ("decode_simt.cu",),
+}
+COMMON_SOURCES = ("split_merge.cuh", "internal.h", "common.cuh")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
+
+
+def kernel_source_hash(kernel):
+    """Hash of the source files a decode kernel is compiled from (first 16 hex digits)."""
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel] + COMMON_SOURCES:
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload, kernel, cfg):
+    """dram__bytes_read.sum + dram__bytes_write.sum per launch of `kernel` on this workload,
+    from the recorded capture of the same kernel source; scaled by tokens processed when the
+    capture ran a smaller batch or T. None when no capture matches the current source."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        entries = json.load(f).get("entries", [])
+    src = kernel_source_hash(kernel)
+    for e in entries:
+        if e.get("workload") == workload and e.get("kernel") == kernel and e.get("source_sha256") == src:
+            scale = (cfg.batch * cfg.T) / (e["batch"] * e["tokens"])
+            return int(round(e["dram_bytes"] * scale))
+    return None
 
 
 # ---------------------------------------------------------------------------
@@ -204,10 +244,18 @@ class GpuWorkload:
 
     @property
     def launches_per_step(self):
-        # append (K and V in one launch) + decode with the split merge inside; the absorbed
-        # and CUDA-core kernels add a query-preparation launch
-        tc = self.cfg.mode == "rope" and self.cfg.latent_dtype in ("f16", "bf16")
-        return 2 if tc else 3
+        # one append launch (K and V together) + the decode call's own launches: the split
+        # merge runs inside the decode kernel; the absorbed and CUDA-core kernels add a
+        # query-preparation launch
+        kernel, _, launches = self.attn.plan(self.cfg.T, self.cfg.batch, self.cfg.T)
+        return 1 + launches
+
+    @property
+    def kernel_name(self):
+        from rank_kv_cache_gb300 import palu as P
+        kernel = self.attn.plan(self.cfg.T, self.cfg.batch, self.cfg.T)[0]
+        return {P.PALU_KERNEL_TC_ROPE: "decode_tc_kernel", P.PALU_KERNEL_TMA_ABSORBED: "decode_abs_kernel",
+                P.PALU_KERNEL_SIMT: "decode_simt_kernel"}[kernel]
 
 
 def run_gpu(args, cfg, name):
@@ -291,6 +339,8 @@ def run_gpu(args, cfg, name):
 
     peaks, peaks_src = load_peaks()
     roof = roofline_for(cfg, work, kernel_ms, peaks, peaks_src, long_step=ms_per_step > 10.0)
+    roof["kernel"] = wl.kernel_name
+    roof["traffic"] = recorded_traffic(name, wl.kernel_name, cfg)
     gb = work["decode_bytes"] / 1e9
     result = {
         "metric": METRIC,
@@ -379,7 +429,7 @@ def cpu_baseline(cfg, work, budget_s=12.0):
     sample = OracleSample(cfg)
     done = 0
     t0 = time.perf_counter()
-    while time.perf_counter() - t0 < budget_s and done < 4 * len(sample.heads):
+    while time.perf_counter() - t0 < budget_s:
         h = sample.heads[done % len(sample.heads)]
         sample.run([h])
         done += 1

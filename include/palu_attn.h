@@ -175,6 +175,26 @@ palu_status_t palu_decode_attn(palu_attn_t h, const void* q, const palu_cache* c
                                palu_stream_t stream);
 
 /*
+ * Which kernel palu_decode_attn would launch for this shape, and its split-T plan.
+ * Host-only: reads no device memory and queues nothing. A convenience for tests and
+ * benchmarks; the pages' statement of the problem has no such call.
+ *   cache_capacity  tokens per batch row of the cache that would be passed
+ *   batch, max_seq_len  as for palu_decode_attn (same limits)
+ *   kernel    out: a palu_kernel_t
+ *   n_splits  out: split-T ranges per (batch row, head group); 1 = no split
+ *   launches  out: kernel launches the decode call makes (the query preparation
+ *             of the CUDA-core and absorbed kernels counts as one)
+ * PALU_ERR_INVALID_ARG on a NULL pointer or an argument outside the limits.
+ */
+typedef enum {
+  PALU_KERNEL_TC_ROPE = 1,       /* tensor-core rebuild + RoPE (fp16, bf16, int4 latents) */
+  PALU_KERNEL_TMA_ABSORBED = 2,  /* absorbed query, TMA-streamed latents (fp16, bf16) */
+  PALU_KERNEL_SIMT = 3           /* CUDA-core kernel: every other supported combination */
+} palu_kernel_t;
+palu_status_t palu_decode_plan(palu_attn_t h, int64_t cache_capacity, int batch, int64_t max_seq_len,
+                               int* kernel, int* n_splits, int* launches);
+
+/*
  * Absorbed-mode decode for callers that cannot allocate device memory (a plugin
  * whose host owns every allocation, an engine with a fixed memory plan, code that
  * must not allocate once serving starts). The pages have no counterpart to it.

@@ -297,6 +297,72 @@ palu_status_t palu_append_latents(palu_attn_t h, const palu_cache* cache, const 
   return e == cudaSuccess ? PALU_OK : PALU_ERR_CUDA;
 }
 
+// Shape, type and workspace fields of a decode launch (the per-call pointers are set by the caller).
+static void fill_args(const palu_attn* h, const palu_cache* cache, int batch, int64_t max_seq_len, DecodeArgs& a) {
+  const palu_attn_desc& d = h->d;
+  a.hk = cache->hk;
+  a.hv = cache->hv;
+  a.k_scale = static_cast<const __half*>(cache->k_scale);
+  a.v_scale = static_cast<const __half*>(cache->v_scale);
+  a.capacity = cache->capacity;
+  a.n_heads = d.n_heads;
+  a.n_g = h->n_g;
+  a.s = d.group_size;
+  a.dh = d.head_dim;
+  a.rk = d.rank_k;
+  a.rv = d.rank_v;
+  a.k_dtype = to_dt(d.k_dtype);
+  a.v_dtype = to_dt(d.v_dtype);
+  a.bk_dtype = to_dt(d.bk_dtype);
+  a.batch = batch;
+  a.max_seq_len = (int)max_seq_len;
+  a.max_pos = h->L.max_pos;
+  a.qbuf = reinterpret_cast<const float*>(h->ws + h->L.qbuf);
+  a.bk = h->ws + h->L.bk;
+  a.bkt = h->ws + h->L.bkt;
+  a.rope = reinterpret_cast<const float2*>(h->ws + h->L.rope);
+  a.phase = reinterpret_cast<const uint64_t*>(h->ws + h->L.phase);
+  a.q_dtype = to_dt(d.q_dtype);
+  a.qscale = float(1.4426950408889634 / sqrt((double)d.head_dim));
+  a.part_o = reinterpret_cast<float*>(h->ws + h->L.part_o);
+  a.part_ml = reinterpret_cast<float2*>(h->ws + h->L.part_ml);
+  a.err = reinterpret_cast<ErrWord*>(h->ws + h->L.err);
+  a.counters = reinterpret_cast<unsigned*>(h->ws + h->L.counters);  // the decode kernels merge the splits
+}
+
+// Kernel choice and split-T plan: tensor-core rebuild (RoPE; fp16, bf16 and int4 latents),
+// TMA stream (absorbed, fp16/bf16), CUDA-core kernel for everything else (fp32 latents, int4
+// absorbed, other shapes). Sets a.n_splits / a.tiles_per_split; returns a palu_kernel_t.
+static int plan_decode(const palu_attn* h, DecodeArgs& a) {
+  const bool rope = h->d.mode == PALU_MODE_ROPE;
+  const int kernel = (rope && tc_supported(a)) ? PALU_KERNEL_TC_ROPE
+                     : (!rope && abs_supported(a)) ? PALU_KERNEL_TMA_ABSORBED
+                                                   : PALU_KERNEL_SIMT;
+  const int tile = kernel == PALU_KERNEL_TC_ROPE ? tc_tile_tokens()
+                   : kernel == PALU_KERNEL_TMA_ABSORBED ? abs_stage_tokens()
+                                                        : kSimtTile;
+  const int64_t tiles = a.max_seq_len > 0 ? (a.max_seq_len + tile - 1) / tile : 1;
+  const int64_t units = (int64_t)a.batch * h->n_g * (kernel == PALU_KERNEL_TC_ROPE ? tc_ctas_per_group(a) : 1);
+  plan_splits(tiles, units, kernel == PALU_KERNEL_SIMT ? 2 * h->sm_count : h->sm_count, h->L.max_splits,
+              &a.n_splits, &a.tiles_per_split);
+  return kernel;
+}
+
+palu_status_t palu_decode_plan(palu_attn_t h, int64_t cache_capacity, int batch, int64_t max_seq_len, int* kernel,
+                               int* n_splits, int* launches) {
+  if (!h || !kernel || !n_splits || !launches) return PALU_ERR_INVALID_ARG;
+  if (cache_capacity <= 0 || batch <= 0 || batch > h->d.max_batch) return PALU_ERR_INVALID_ARG;
+  if (max_seq_len < 0 || max_seq_len > h->d.max_tokens || max_seq_len > cache_capacity) return PALU_ERR_INVALID_ARG;
+  palu_cache c{};
+  c.capacity = cache_capacity;
+  DecodeArgs a{};
+  fill_args(h, &c, batch, max_seq_len, a);
+  *kernel = plan_decode(h, a);
+  *n_splits = a.n_splits;
+  *launches = *kernel == PALU_KERNEL_TC_ROPE ? 1 : 2;  // the other kernels read a prepared query
+  return PALU_OK;
+}
+
 palu_status_t palu_decode_attn(palu_attn_t h, const void* q, const palu_cache* cache, const int32_t* seq_lens,
                                const int32_t* positions, const int32_t* q_pos, int batch, int64_t max_seq_len,
                                float* out, float* lse, palu_stream_t stream) {
@@ -312,57 +378,21 @@ palu_status_t palu_decode_attn(palu_attn_t h, const void* q, const palu_cache* c
   if (cudaSetDevice(h->device) != cudaSuccess) return PALU_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
-  const palu_attn_desc& d = h->d;
   DecodeArgs a{};
-  a.hk = cache->hk;
-  a.hv = cache->hv;
-  a.k_scale = static_cast<const __half*>(cache->k_scale);
-  a.v_scale = static_cast<const __half*>(cache->v_scale);
-  a.capacity = cache->capacity;
-  a.n_heads = d.n_heads;
-  a.n_g = h->n_g;
-  a.s = d.group_size;
-  a.dh = d.head_dim;
-  a.rk = d.rank_k;
-  a.rv = d.rank_v;
-  a.k_dtype = to_dt(d.k_dtype);
-  a.v_dtype = to_dt(d.v_dtype);
-  a.bk_dtype = to_dt(d.bk_dtype);
+  fill_args(h, cache, batch, max_seq_len, a);
   a.seq_lens = seq_lens;
-  a.positions = (d.mode == PALU_MODE_ROPE) ? positions : nullptr;
-  a.batch = batch;
-  a.max_seq_len = (int)max_seq_len;
-  a.max_pos = h->L.max_pos;
-  a.qbuf = reinterpret_cast<const float*>(h->ws + h->L.qbuf);
-  a.bk = h->ws + h->L.bk;
-  a.bkt = h->ws + h->L.bkt;
-  a.rope = reinterpret_cast<const float2*>(h->ws + h->L.rope);
-  a.phase = reinterpret_cast<const uint64_t*>(h->ws + h->L.phase);
+  a.positions = (h->d.mode == PALU_MODE_ROPE) ? positions : nullptr;
   a.q = q;
-  a.q_dtype = to_dt(d.q_dtype);
   a.q_pos = q_pos;
-  a.qscale = float(1.4426950408889634 / sqrt((double)d.head_dim));
-  a.part_o = reinterpret_cast<float*>(h->ws + h->L.part_o);
-  a.part_ml = reinterpret_cast<float2*>(h->ws + h->L.part_ml);
-  a.err = reinterpret_cast<ErrWord*>(h->ws + h->L.err);
-  a.counters = reinterpret_cast<unsigned*>(h->ws + h->L.counters);  // the decode kernels merge the splits
   a.out = out;
   a.lse = lse;
-
-  const int mode = d.mode == PALU_MODE_ROPE ? kRope : kAbsorbed;
-  // kernel choice: tensor-core rebuild (RoPE; fp16, bf16 and int4 latents), TMA stream (absorbed,
-  // fp16/bf16), CUDA-core kernel for everything else (fp32 latents, int4 absorbed, other shapes)
-  const bool use_tc = mode == kRope && tc_supported(a);
-  const bool use_abs = mode == kAbsorbed && abs_supported(a);
-  const int tile = use_tc ? tc_tile_tokens() : use_abs ? abs_stage_tokens() : kSimtTile;
-  const int64_t tiles = max_seq_len > 0 ? (max_seq_len + tile - 1) / tile : 1;
-  const int64_t units = (int64_t)batch * h->n_g * (use_tc ? tc_ctas_per_group(a) : 1);
-  plan_splits(tiles, units, (use_tc || use_abs) ? h->sm_count : 2 * h->sm_count, h->L.max_splits, &a.n_splits,
-              &a.tiles_per_split);
+  const int mode = h->d.mode == PALU_MODE_ROPE ? kRope : kAbsorbed;
+  const int kernel = plan_decode(h, a);
+  const bool use_tc = kernel == PALU_KERNEL_TC_ROPE, use_abs = kernel == PALU_KERNEL_TMA_ABSORBED;
 
   // the tensor-core kernel rotates its query itself; the other kernels read the prepared buffer
   cudaError_t e = use_tc ? cudaSuccess
-                         : launch_qprep(mode, q, to_dt(d.q_dtype), a, q_pos, a.qscale, const_cast<float*>(a.qbuf), s);
+                         : launch_qprep(mode, q, a.q_dtype, a, q_pos, a.qscale, const_cast<float*>(a.qbuf), s);
   cudaEvent_t* tr = (e == cudaSuccess) ? trace_slot(h) : nullptr;
   if (tr) e = cudaEventRecord(tr[0], s);
   if (e == cudaSuccess)

@@ -22,6 +22,7 @@ PALU_OK, PALU_ERR_INVALID_ARG, PALU_ERR_UNSUPPORTED, PALU_ERR_CUDA, PALU_ERR_DEV
     PALU_ERR_WORKSPACE = range(7)
 PALU_F32, PALU_F16, PALU_BF16, PALU_INT4 = range(4)
 PALU_MODE_ROPE, PALU_MODE_ABSORBED = 0, 1
+PALU_KERNEL_TC_ROPE, PALU_KERNEL_TMA_ABSORBED, PALU_KERNEL_SIMT = 1, 2, 3
 
 DTYPES = {"f32": PALU_F32, "f16": PALU_F16, "bf16": PALU_BF16, "int4": PALU_INT4}
 MODES = {"rope": PALU_MODE_ROPE, "absorbed": PALU_MODE_ABSORBED}
@@ -29,7 +30,7 @@ MODES = {"rope": PALU_MODE_ROPE, "absorbed": PALU_MODE_ABSORBED}
 # every symbol include/palu_attn.h declares
 EXPORTS = ("palu_attn_workspace_size", "palu_attn_create", "palu_append_latents", "palu_decode_attn",
            "palu_destroy", "palu_attn_check", "palu_status_string", "palu_debug_dequant",
-           "palu_attn_trace_enable", "palu_attn_trace_read", "palu_decode_attn_noalloc")
+           "palu_attn_trace_enable", "palu_attn_trace_read", "palu_decode_attn_noalloc", "palu_decode_plan")
 PALU_TRACE_CAPACITY = 4096
 
 
@@ -71,6 +72,7 @@ def _load():
         "palu_attn_trace_read": (I, [P, ctypes.POINTER(I), ctypes.POINTER(ctypes.c_double)]),
         "palu_decode_attn_noalloc": (I, [ctypes.POINTER(palu_attn_desc), P, P, ctypes.POINTER(palu_cache), P, I,
                                          I64, P, P, P]),
+        "palu_decode_plan": (I, [P, I64, I, I64, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(I)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -141,6 +143,14 @@ def palu_decode_attn_noalloc(desc: palu_attn_desc, bk: int, q: int, cache: palu_
     """Absorbed-mode decode with the library's fixed device scratch (no allocation anywhere)."""
     return _lib.palu_decode_attn_noalloc(ctypes.byref(desc), bk, q, ctypes.byref(cache), seq_lens, batch,
                                          max_seq_len, out, lse, stream)
+
+
+def palu_decode_plan(h, cache_capacity: int, batch: int, max_seq_len: int):
+    """(status, kernel, n_splits, launches) of the decode call for this shape; host-only."""
+    k, n, l = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    st = _lib.palu_decode_plan(h, cache_capacity, batch, max_seq_len, ctypes.byref(k), ctypes.byref(n),
+                               ctypes.byref(l))
+    return st, k.value, n.value, l.value
 
 
 def check(status: int, what: str = "palu") -> None:
@@ -260,6 +270,13 @@ class PaluAttention:
                               _ptr(q_pos), B, int(max_seq_len), _ptr(out), _ptr(lse), _stream_handle(stream))
         check(st, "palu_decode_attn")
         return out
+
+    def plan(self, cache_capacity, batch, max_seq_len):
+        """(kernel, n_splits, launches) that decode() would use; host-only."""
+        st, kernel, n_splits, launches = palu_decode_plan(self.handle, int(cache_capacity), int(batch),
+                                                          int(max_seq_len))
+        check(st, "palu_decode_plan")
+        return kernel, n_splits, launches
 
     def check_device(self, stream=None):
         check(palu_attn_check(self.handle, _stream_handle(stream)), "palu_attn_check")

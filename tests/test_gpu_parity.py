@@ -171,3 +171,21 @@ def test_full_size_sampled_heads(cid, T):
     heads = _sample_heads(cfg.batch, cfg.n_heads)
     ref, lse_ref = c.run_oracle(heads=heads)
     assert_close(out, ref, lse, lse_ref, heads=heads)
+
+
+@pytest.mark.parametrize("cid,kernel", [(1, "SIMT"), (2, "TC_ROPE"), (3, "TC_ROPE"), (4, "TMA_ABSORBED"),
+                                        (5, "TC_ROPE")])
+def test_kernel_choice_per_workload(cid, kernel):
+    # the fast kernels must be the ones the full-size workloads run on
+    import torch
+    from rank_kv_cache_gb300 import palu as P
+    cfg = gen.CONFIGS[cid]
+    bk = torch.zeros((cfg.n_groups, cfg.rank, cfg.group_size * cfg.head_dim),
+                     dtype={"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[cfg.bk_dtype],
+                     device="cuda")
+    attn = P.PaluAttention(bk, n_heads=cfg.n_heads, head_dim=cfg.head_dim, group_size=cfg.group_size,
+                           rank_k=cfg.rank, rank_v=cfg.rank, latent_dtype=cfg.latent_dtype, q_dtype=cfg.q_dtype,
+                           mode=cfg.mode, max_batch=cfg.batch, max_tokens=cfg.T)
+    got, n_splits, launches = attn.plan(cfg.T, cfg.batch, cfg.T)
+    assert got == getattr(P, "PALU_KERNEL_" + kernel)
+    assert n_splits >= 1 and launches == (1 if kernel == "TC_ROPE" else 2)
