@@ -79,7 +79,7 @@ struct Lay {
   static constexpr int kOffPk = kOffA + kStages * kAStage;
   static constexpr int kOffV = kOffPk + kPStages * kPStage;
   static constexpr int kOffBar = kOffV + kVSlots * kVSlot;
-  static constexpr int kNumBars = 48;
+  static constexpr int kNumBars = 52;
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;
   static constexpr int kOffQ = (kOffMisc + 16 + 15) & ~15;     // float4 [kHalf]: (qa0, qa1, qb0, qb1)
   static constexpr int kOffF = kOffQ + kHalf * 16;             // uint64 [kHalf]
@@ -168,8 +168,9 @@ __device__ __forceinline__ void setmaxnreg_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
-// VT = value-latent storage (__half, __nv_bfloat16, or Int4); I4 = int4 latents (fp16 MMA operands)
-template <typename VT, bool I4>
+// VT = value-latent storage (__half, __nv_bfloat16, or Int4); I4 = int4 latents (fp16 MMA operands);
+// FOLD = the rotated query is folded into the B operand (fp16 operands only, see below)
+template <typename VT, bool I4, bool FOLD>
 __global__ void __launch_bounds__(Lay<I4>::kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_hk, const __grid_constant__ CUtensorMap tm_hv,
                      const __grid_constant__ CUtensorMap tm_b, const TcParams P) {
@@ -197,6 +198,7 @@ __global__ void __launch_bounds__(Lay<I4>::kThreads, 1)
   uint64_t* pfull = bars + 36;            // [kPStages]
   uint64_t* pempty = bars + 40;           // [kPStages]
   uint64_t* mma_done = bars + 44;
+  uint64_t* bready = bars + 45;           // [kChunks] B chunk folded (FOLD only)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + LY::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + LY::kOffMisc + 4);
   float4* qs = reinterpret_cast<float4*>(smem + LY::kOffQ);
@@ -237,6 +239,7 @@ __global__ void __launch_bounds__(Lay<I4>::kThreads, 1)
       tc::mbar_init(&pempty[i], 4);   // converter warps
     }
     tc::mbar_init(mma_done, 1);
+    for (int i = 0; i < kChunks; ++i) tc::mbar_init(&bready[i], 8);  // eight softmax/PV warps
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
@@ -356,7 +359,7 @@ __global__ void __launch_bounds__(Lay<I4>::kThreads, 1)
           tc::tc_fence_after();
           const uint32_t d = tmem_base + buf * kN;
           for (int kc = 0; kc < kChunks; ++kc) {
-            if (it == 0 && !tc::mbar_wait_bounded(&bfull[kc], 0, abort_flag, kWaitNs)) {
+            if (it == 0 && !tc::mbar_wait_bounded(FOLD ? &bready[kc] : &bfull[kc], 0, abort_flag, kWaitNs)) {
               ok = false;
               break;
             }
@@ -463,19 +466,35 @@ __global__ void __launch_bounds__(Lay<I4>::kThreads, 1)
           __sincosf(float(int32_t(top)) * kTurnToRad, &sn[u], &cs[u]);
         }
         tc::tmem_ld_wait();
+        if constexpr (FOLD) {
+          // the MMA produced X_k = q_a k_a + q_b k_b and Y_k = q_b k_a - q_a k_b directly
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const float4 q4 = qs[a0 + u];     // (qa0, qa1, qb0, qb1)
-          const float ka0 = __uint_as_float(k0[u]), kb0 = __uint_as_float(k0[16 + u]);
-          const float ka1 = __uint_as_float(k1[u]), kb1 = __uint_as_float(k1[16 + u]);
-          const float t0v = fmaf(q4.x, ka0, q4.z * kb0), v0 = fmaf(q4.z, ka0, -q4.x * kb0);
-          const float t1v = fmaf(q4.y, ka1, q4.w * kb1), v1 = fmaf(q4.w, ka1, -q4.y * kb1);
-          if (u & 1) {
-            s0b = fmaf(sn[u], v0, fmaf(cs[u], t0v, s0b));
-            s1b = fmaf(sn[u], v1, fmaf(cs[u], t1v, s1b));
-          } else {
-            s0a = fmaf(sn[u], v0, fmaf(cs[u], t0v, s0a));
-            s1a = fmaf(sn[u], v1, fmaf(cs[u], t1v, s1a));
+          for (int u = 0; u < 16; ++u) {
+            const float x0 = __uint_as_float(k0[u]), y0 = __uint_as_float(k0[16 + u]);
+            const float x1 = __uint_as_float(k1[u]), y1 = __uint_as_float(k1[16 + u]);
+            if (u & 1) {
+              s0b = fmaf(sn[u], y0, fmaf(cs[u], x0, s0b));
+              s1b = fmaf(sn[u], y1, fmaf(cs[u], x1, s1b));
+            } else {
+              s0a = fmaf(sn[u], y0, fmaf(cs[u], x0, s0a));
+              s1a = fmaf(sn[u], y1, fmaf(cs[u], x1, s1a));
+            }
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            const float4 q4 = qs[a0 + u];     // (qa0, qa1, qb0, qb1)
+            const float ka0 = __uint_as_float(k0[u]), kb0 = __uint_as_float(k0[16 + u]);
+            const float ka1 = __uint_as_float(k1[u]), kb1 = __uint_as_float(k1[16 + u]);
+            const float t0v = fmaf(q4.x, ka0, q4.z * kb0), v0 = fmaf(q4.z, ka0, -q4.x * kb0);
+            const float t1v = fmaf(q4.y, ka1, q4.w * kb1), v1 = fmaf(q4.w, ka1, -q4.y * kb1);
+            if (u & 1) {
+              s0b = fmaf(sn[u], v0, fmaf(cs[u], t0v, s0b));
+              s1b = fmaf(sn[u], v1, fmaf(cs[u], t1v, s1b));
+            } else {
+              s0a = fmaf(sn[u], v0, fmaf(cs[u], t0v, s0a));
+              s1a = fmaf(sn[u], v1, fmaf(cs[u], t1v, s1a));
+            }
           }
         }
       }
@@ -508,6 +527,47 @@ __global__ void __launch_bounds__(Lay<I4>::kThreads, 1)
     for (int c = 0; c < 4; ++c) acc0[c] = acc1[c] = 0.f;
     bool aborted = false;  // warpgroup-uniform: only ever set from a barrier-OR
     bool broken = false;   // this warp's own H_v wait gave up
+    if (FOLD && n_tiles > 0) {  // (B_k is loaded only when the CTA has tokens)
+      // Fold the rotated query into B_k^T, in place, before the first MMA: for head j and
+      // rotation pair k, rows a = 128 j + k and b = a + 64 of B_k^T become
+      //   U = q_a B_a + q_b B_b   and   W = q_b B_a - q_a B_b,
+      // so the MMA yields X_k = q_a k_a + q_b k_b and Y_k = q_b k_a - q_a k_b per token and the
+      // rotated score is sum_k cos X_k + sin Y_k. Rows a and b share their swizzle phase (a = b
+      // mod 8), so element m of both rows sits at the same offset in its row.
+      const int t2 = threadIdx.x - 3 * kWg;  // 0..255
+      for (int kc = 0; kc < kChunks; ++kc) {
+        if (!tc::mbar_wait_bounded(&bfull[kc], 0, abort_flag, kWaitNs)) broken = true;
+        if (!broken) {
+          uint8_t* chunk = smem + LY::kOffB + kc * kBChunk;
+#pragma unroll
+          for (int rep = 0; rep < 4; ++rep) {
+            const int job = t2 + rep * 2 * kWg;          // 0..1023: (head, pair, 16-byte chunk)
+            const int c = job & 7, k = (job >> 3) & (kHalf - 1), j = job >> 9;
+            const int ra = j * kDh + k;
+            const float4 q4 = qs[k];
+            const float qa = j ? q4.y : q4.x, qb = j ? q4.w : q4.z;
+            uint4* pa = reinterpret_cast<uint4*>(chunk + ra * 128 + ((c ^ (ra & 7)) << 4));
+            uint4* pb = reinterpret_cast<uint4*>(chunk + (ra + kHalf) * 128 + ((c ^ (ra & 7)) << 4));
+            uint4 va = *pa, vb = *pb;
+            __half2* ha = reinterpret_cast<__half2*>(&va);
+            __half2* hb = reinterpret_cast<__half2*>(&vb);
+#pragma unroll
+            for (int e2 = 0; e2 < 4; ++e2) {
+              const float2 ba = __half22float2(ha[e2]), bb = __half22float2(hb[e2]);
+              const float2 uu = make_float2(fmaf(qa, ba.x, qb * bb.x), fmaf(qa, ba.y, qb * bb.y));
+              const float2 ww = make_float2(fmaf(qb, ba.x, -qa * bb.x), fmaf(qb, ba.y, -qa * bb.y));
+              ha[e2] = __float22half2_rn(uu);
+              hb[e2] = __float22half2_rn(ww);
+            }
+            *pa = va;
+            *pb = vb;
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor cores
+        }
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&bready[kc]);
+      }
+    }
     float vs_next = 1.f;
     if constexpr (I4)
       if (t_begin + ei < t_end) vs_next = __half2float(a.v_scale[((int64_t)row0 + t_begin + ei) * a.n_g + g]);
@@ -737,10 +797,10 @@ bool tc_supported(const DecodeArgs& a) {
 int tc_tile_tokens() { return kTile; }
 int tc_ctas_per_group(const DecodeArgs& a) { return a.s / kHeads; }
 
-template <typename VT, bool I4>
+template <typename VT, bool I4, bool FOLD>
 cudaError_t launch_variant(const CUtensorMap& tm_hk, const CUtensorMap& tm_hv, const CUtensorMap& tm_b,
                            const TcParams& P, cudaStream_t st) {
-  auto kern = decode_tc_kernel<VT, I4>;
+  auto kern = decode_tc_kernel<VT, I4, FOLD>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<I4>::kSmemAlloc);
   if (e != cudaSuccess) return e;
   dim3 grid(P.a.n_splits * P.hp_count, P.a.n_g, P.a.batch);
@@ -788,9 +848,11 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st) {
   P.a = a;
   P.hp_count = a.s / kHeads;
   P.bf16 = a.k_dtype == kBF16;
-  if (i4) return launch_variant<Int4, true>(tm_hk, tm_hv, tm_b, P, st);
-  if (a.k_dtype == kBF16) return launch_variant<__nv_bfloat16, false>(tm_hk, tm_hv, tm_b, P, st);
-  return launch_variant<__half, false>(tm_hk, tm_hv, tm_b, P, st);
+  // fp16 operands carry the folded query with 11-bit precision; bf16 ones (8-bit) would not,
+  // so the bf16 kernel rebuilds K exactly and applies the query in the epilogue
+  if (i4) return launch_variant<Int4, true, true>(tm_hk, tm_hv, tm_b, P, st);
+  if (a.k_dtype == kBF16) return launch_variant<__nv_bfloat16, false, false>(tm_hk, tm_hv, tm_b, P, st);
+  return launch_variant<__half, false, true>(tm_hk, tm_hv, tm_b, P, st);
 }
 
 }  // namespace palu
