@@ -50,7 +50,6 @@ constexpr int kChunks = kRank / kKChunk;         // 4
 constexpr int kAStage = kTile * kKChunk * 2;     // 16 KB fp16 operand chunk
 constexpr int kBChunk = kN * kKChunk * 2;        // 32 KB
 constexpr int kBBytes = kBChunk * kChunks;       // 128 KB
-constexpr int kVHalf = kRank / 2;                // value columns per softmax/PV warpgroup
 constexpr int kWg = 128;                         // threads per warpgroup
 constexpr uint32_t kTmemCols = 512;              // two N=256 fp32 accumulators
 constexpr uint64_t kWaitNs = 1000000000ull;      // 1 s per wait
@@ -89,11 +88,11 @@ struct Lay {
   static constexpr int kOffL = kOffP + 2 * kTile * 8;          // float2 [2 wg][4]
   static constexpr int kSmemBytes = kOffL + 2 * 4 * 8;
   static constexpr int kSmemAlloc = kSmemBytes + 1024;
-  static constexpr int kOffO = kOffV;                          // [2 wg][4][kHeads][kVHalf] floats
+  static constexpr int kOffO = kOffV;                          // [8 warps][kHeads][kRank] floats
   static_assert(kWg * kRegsCtl + 2 * kWg * kRegsScore + 2 * kWg * kRegsPv + (I4 ? kWg * kRegsConv : 0) <=
                     kThreads * kLaunchRegs,
                 "register split");
-  static_assert(2 * 4 * kHeads * kVHalf * 4 <= kVSlots * kVSlot, "output reduction fits the H_v ring");
+  static_assert(8 * kHeads * kRank * 4 <= kVSlots * kVSlot, "output reduction fits the H_v ring");
   static_assert(kHeads * (256 + 2) * 4 <= kVSlots * kVSlot, "split-merge scratch fits the H_v ring");
   static_assert(kSmemAlloc <= 232448, "shared memory budget");
 };
@@ -104,29 +103,30 @@ struct TcParams {
   int bf16;       // MMA operand type
 };
 
-template <typename VT>
-__device__ __forceinline__ void unpack4(const uint2& u, float* h);
-template <>
-__device__ __forceinline__ void unpack4<__half>(const uint2& u, float* h) {
-  const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
-  const float2 y = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
-  h[0] = x.x;
-  h[1] = x.y;
-  h[2] = y.x;
-  h[3] = y.y;
+// d += a.lo16 * b.byte0 + a.hi16 * b.byte1 (lo) / b.byte2, b.byte3 (hi), unsigned
+__device__ __forceinline__ uint32_t dp2a_lo(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("dp2a.lo.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
 }
-template <>
-__device__ __forceinline__ void unpack4<__nv_bfloat16>(const uint2& u, float* h) {
-  h[0] = __uint_as_float(u.x << 16);
-  h[1] = __uint_as_float(u.x & 0xffff0000u);
-  h[2] = __uint_as_float(u.y << 16);
-  h[3] = __uint_as_float(u.y & 0xffff0000u);
+__device__ __forceinline__ uint32_t dp2a_hi(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("dp2a.hi.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
 }
-// four signed 4-bit codes (element order: low nibble first) as floats
-__device__ __forceinline__ void unpack4_int4(uint32_t two_bytes, float* h) {
+
+// eight fp16 / bf16 values (16 bytes) as four float pairs
+__device__ __forceinline__ void vt8_to_float2x4(const uint4& u, float2* f, __half) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-  for (int i = 0; i < 4; ++i) h[i] = float(int32_t(two_bytes << (28 - 4 * i)) >> 28);
+  for (int j = 0; j < 4; ++j) f[j] = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
 }
+__device__ __forceinline__ void vt8_to_float2x4(const uint4& u, float2* f, __nv_bfloat16) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) f[j] = make_float2(__uint_as_float(w[j] << 16), __uint_as_float(w[j] & 0xffff0000u));
+}
+
 // eight signed 4-bit codes of a 32-bit word (element 2j = low nibble of byte j) as eight
 // exact fp16 values: each nibble biased by 8 is placed under the fp16 exponent of 1024
 // (0x64xx), and 1032 is subtracted.
@@ -509,8 +509,10 @@ __global__ void __launch_bounds__(Lay<I4>::kThreads, 1)
   } else if (wg <= 4) {
     // ------------------------------------------------------------ softmax / PV warpgroups
     // Both warpgroups run the same online softmax over the tile's 128 scores (summing the two
-    // partial scores); warpgroup Y accumulates p H_v for value columns 128Y..128Y+127. For
-    // int4 latents p is multiplied by the token's value scale before it weights the codes.
+    // partial scores). For p H_v every lane owns 8 of the 256 value columns (lane 8 .. lane 8 + 7)
+    // and the eight warps share out each H_v chunk's tokens; packed f32x2 FMAs update both
+    // heads' column pairs. For int4 latents p is multiplied by the token's value scale before
+    // it weights the codes.
     setmaxnreg_dec<LY::kRegsPv>();
     const int Y = wg - 3;
     const int e = warp & 3;                  // warp within the warpgroup
@@ -519,12 +521,13 @@ __global__ void __launch_bounds__(Lay<I4>::kThreads, 1)
     float2* red = reinterpret_cast<float2*>(smem + LY::kOffRed) + Y * 4;
     float2* pbuf = reinterpret_cast<float2*>(smem + LY::kOffP) + Y * kTile;
     float2* lred = reinterpret_cast<float2*>(smem + LY::kOffL) + Y * 4;
-    float* ored = reinterpret_cast<float*>(smem + LY::kOffO) + Y * (4 * kHeads * kVHalf);
+    float* ored = reinterpret_cast<float*>(smem + LY::kOffO);  // [8 warps][kHeads][kRank] at the end
+    const int w8 = Y * 4 + e;                                   // warp among the eight
     float m_run0 = -INFINITY, m_run1 = -INFINITY;
     float l0 = 0.f, l1 = 0.f;
-    float acc0[4], acc1[4];
+    float2 acc0[4], acc1[4];     // columns (lane 8 + 2 j, lane 8 + 2 j + 1) of head 0 / head 1
 #pragma unroll
-    for (int c = 0; c < 4; ++c) acc0[c] = acc1[c] = 0.f;
+    for (int c = 0; c < 4; ++c) acc0[c] = acc1[c] = make_float2(0.f, 0.f);
     bool aborted = false;  // warpgroup-uniform: only ever set from a barrier-OR
     bool broken = false;   // this warp's own H_v wait gave up
     if (FOLD && n_tiles > 0) {  // (B_k is loaded only when the CTA has tokens)
@@ -613,72 +616,119 @@ __global__ void __launch_bounds__(Lay<I4>::kThreads, 1)
       pbuf[ei] = I4 ? make_float2(p0 * vsc, p1 * vsc) : make_float2(p0, p1);
       tc::named_bar(bar, kWg);
 
+      {
+        const float2 a0 = make_float2(al0, al0), a1 = make_float2(al1, al1);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        acc0[c] *= al0;
-        acc1[c] *= al1;
+        for (int c = 0; c < 4; ++c) {
+          acc0[c] = __fmul2_rn(acc0[c], a0);
+          acc1[c] = __fmul2_rn(acc1[c], a1);
+        }
       }
       if constexpr (I4) {
-        // p H_v over 64-token chunks of packed rows; warp e takes 16 tokens of each chunk and
-        // lane owns the codes of columns 128Y + 4 lane .. 128Y + 4 lane + 3 (two bytes)
+        // p H_v on the integer codes. Warp w8 owns tokens 64 ch + 8 w8 .. 64 ch + 8 w8 + 7 of
+        // chunks ch = 0, 1 (16 tokens); lane l quantises the weight p' = p * v_scale of token
+        // (l & 15) for head l >> 4 to 15 bits against the largest of the warp's 16 weights of that
+        // head, q = rint(p' * 32767 / S). Then dp2a multiplies two tokens' weights by their biased
+        // codes (code + 8, bytes) per column, with exact int32 sums; subtracting 8 * sum(q) removes
+        // the bias. The rounding of q errs by at most S / 65534 per weight.
+        const int jt = lane & 15, hh = lane >> 4;
+        const int tkq = (jt >> 3) * kVTok + w8 * 8 + (jt & 7);
+        const float2 pq = pbuf[tkq];
+        const float pw = hh ? pq.y : pq.x;
+        float smax = pw;
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o));
+        const float inv = smax > 0.f ? 32767.f / smax : 0.f;
+        const uint32_t qv = uint32_t(__float2int_rn(pw * inv));
+        uint32_t qsum = qv;
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) qsum += __shfl_xor_sync(0xffffffffu, qsum, o);
+        const uint32_t qpair = qv | (__shfl_down_sync(0xffffffffu, qv, 1) << 16);  // valid in even lanes
+        uint32_t ai[2][8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) ai[0][c] = ai[1][c] = 0u;
         for (int ch = 0; ch < kVChunks; ++ch) {
           const int vi = it * kVChunks + ch;
           const int slot = vi % kVSlots;
           if (!tc::mbar_wait_bounded(&vfull[slot], (vi / kVSlots) & 1, abort_flag, kWaitNs)) broken = true;
-          const uint8_t* vs = smem + LY::kOffV + slot * kVSlot + (e * 16) * kVRow + Y * (kVHalf / 2) + lane * 2;
-          uint32_t u[16];
+          broken = __any_sync(0xffffffffu, broken);   // warp-uniform before the shuffles below
+          const uint8_t* vs = smem + LY::kOffV + slot * kVSlot + (w8 * 8) * kVRow + lane * 4;
+          uint32_t u[8];
 #pragma unroll
-          for (int k = 0; k < 16; ++k) u[k] = *reinterpret_cast<const uint16_t*>(vs + k * kVRow);
+          for (int k = 0; k < 8; ++k) u[k] = *reinterpret_cast<const uint32_t*>(vs + k * kVRow);
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(&vempty[slot]);
           if (broken) continue;
-          const bool all = t0 + ch * kVTok + e * 16 + 15 < t_end;
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const int tk = ch * kVTok + e * 16 + k;
-            if (all || t0 + tk < t_end) {
-              float h[4];
-              unpack4_int4(u[k], h);
-              const float2 p = pbuf[tk];
+          for (int m = 0; m < 4; ++m) {
+            const uint32_t a0 = __shfl_sync(0xffffffffu, qpair, ch * 8 + 2 * m);
+            const uint32_t a1 = __shfl_sync(0xffffffffu, qpair, 16 + ch * 8 + 2 * m);
+            const uint32_t la = (u[2 * m] ^ 0x88888888u) & 0x0F0F0F0Fu;
+            const uint32_t lb = (u[2 * m + 1] ^ 0x88888888u) & 0x0F0F0F0Fu;
+            const uint32_t ha = ((u[2 * m] >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
+            const uint32_t hb = ((u[2 * m + 1] >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
+            const uint32_t b02 = __byte_perm(la, lb, 0x5140), b46 = __byte_perm(la, lb, 0x7362);
+            const uint32_t b13 = __byte_perm(ha, hb, 0x5140), b57 = __byte_perm(ha, hb, 0x7362);
+            ai[0][0] = dp2a_lo(a0, b02, ai[0][0]);
+            ai[0][2] = dp2a_hi(a0, b02, ai[0][2]);
+            ai[0][4] = dp2a_lo(a0, b46, ai[0][4]);
+            ai[0][6] = dp2a_hi(a0, b46, ai[0][6]);
+            ai[0][1] = dp2a_lo(a0, b13, ai[0][1]);
+            ai[0][3] = dp2a_hi(a0, b13, ai[0][3]);
+            ai[0][5] = dp2a_lo(a0, b57, ai[0][5]);
+            ai[0][7] = dp2a_hi(a0, b57, ai[0][7]);
+            ai[1][0] = dp2a_lo(a1, b02, ai[1][0]);
+            ai[1][2] = dp2a_hi(a1, b02, ai[1][2]);
+            ai[1][4] = dp2a_lo(a1, b46, ai[1][4]);
+            ai[1][6] = dp2a_hi(a1, b46, ai[1][6]);
+            ai[1][1] = dp2a_lo(a1, b13, ai[1][1]);
+            ai[1][3] = dp2a_hi(a1, b13, ai[1][3]);
+            ai[1][5] = dp2a_lo(a1, b57, ai[1][5]);
+            ai[1][7] = dp2a_hi(a1, b57, ai[1][7]);
+          }
+        }
+        if (!broken) {
+          // back to float: sum(q * code) = sum(q * (code + 8)) - 8 sum(q), |.| < 2^22
+          const uint32_t qs0 = __shfl_sync(0xffffffffu, qsum, 0), qs1 = __shfl_sync(0xffffffffu, qsum, 16);
+          const float sc0 = __shfl_sync(0xffffffffu, smax, 0) * (1.f / 32767.f);
+          const float sc1 = __shfl_sync(0xffffffffu, smax, 16) * (1.f / 32767.f);
 #pragma unroll
-              for (int c = 0; c < 4; ++c) {
-                acc0[c] = fmaf(p.x, h[c], acc0[c]);
-                acc1[c] = fmaf(p.y, h[c], acc1[c]);
-              }
-            }
+          for (int c = 0; c < 4; ++c) {
+            const float2 v0 = make_float2(float(int32_t(ai[0][2 * c] - 8u * qs0)), float(int32_t(ai[0][2 * c + 1] - 8u * qs0)));
+            const float2 v1 = make_float2(float(int32_t(ai[1][2 * c] - 8u * qs1)), float(int32_t(ai[1][2 * c + 1] - 8u * qs1)));
+            acc0[c] = __ffma2_rn(v0, make_float2(sc0, sc0), acc0[c]);
+            acc1[c] = __ffma2_rn(v1, make_float2(sc1, sc1), acc1[c]);
           }
         }
       } else {
-        // p H_v over 16-token chunks; warp e takes 4 tokens of each chunk and lane owns
-        // columns 128Y + 4 lane .. 128Y + 4 lane + 3. A warp whose wait gave up skips the
-        // arithmetic; the tile-level barrier-OR above then ends the loop for the warpgroup.
-        for (int ch = 0; ch < kVChunks; ch += 2) {
-          uint2 u[8];
+        // p H_v on fp16/bf16 rows: chunk ch of the tile holds kVTok = 16 tokens and warp w8 takes
+        // two of them. A warp whose wait gave up skips the arithmetic; the tile-level barrier-OR
+        // above then ends the loop for the warpgroup.
+        constexpr int kPer = kVTok / 8;
+        for (int ch = 0; ch < kVChunks; ++ch) {
+          const int vi = it * kVChunks + ch;
+          const int slot = vi % kVSlots;
+          if (!tc::mbar_wait_bounded(&vfull[slot], (vi / kVSlots) & 1, abort_flag, kWaitNs)) broken = true;
+          const uint8_t* vs = smem + LY::kOffV + slot * kVSlot + (w8 * kPer) * kVRow;
+          uint4 u[kPer];
 #pragma unroll
-          for (int c2 = 0; c2 < 2; ++c2) {
-            const int vi = it * kVChunks + ch + c2;
-            const int slot = vi % kVSlots;
-            if (!tc::mbar_wait_bounded(&vfull[slot], (vi / kVSlots) & 1, abort_flag, kWaitNs)) broken = true;
-            const uint8_t* vs = smem + LY::kOffV + slot * kVSlot + (e * 4) * kVRow + (Y * kVHalf + lane * 4) * 2;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) u[c2 * 4 + k] = *reinterpret_cast<const uint2*>(vs + k * kVRow);
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&vempty[slot]);
-          }
+          for (int k = 0; k < kPer; ++k) u[k] = *reinterpret_cast<const uint4*>(vs + k * kVRow + lane * 16);
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&vempty[slot]);
           if (broken) continue;
-          // all eight tokens valid (every tile but the last): no per-token branch
-          const bool all = t0 + (ch + 1) * kVTok + e * 4 + 3 < t_end;
+          const int tk0 = ch * kVTok + w8 * kPer;   // first token (within the tile) of this warp
+          const bool all = t0 + tk0 + kPer - 1 < t_end;
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const int tk = (ch + (k >> 2)) * kVTok + e * 4 + (k & 3);   // token index within the tile
-            if (all || t0 + tk < t_end) {
-              float h[4];
-              unpack4<VT>(u[k], h);
-              const float2 p = pbuf[tk];
+          for (int k = 0; k < kPer; ++k) {
+            if (all || t0 + tk0 + k < t_end) {
+              float2 h[4];
+              vt8_to_float2x4(u[k], h, VT{});
+              const float2 p = pbuf[tk0 + k];
+              const float2 p0 = make_float2(p.x, p.x), p1 = make_float2(p.y, p.y);
 #pragma unroll
               for (int c = 0; c < 4; ++c) {
-                acc0[c] = fmaf(p.x, h[c], acc0[c]);
-                acc1[c] = fmaf(p.y, h[c], acc1[c]);
+                acc0[c] = __ffma2_rn(p0, h[c], acc0[c]);
+                acc1[c] = __ffma2_rn(p1, h[c], acc1[c]);
               }
             }
           }
@@ -686,24 +736,26 @@ __global__ void __launch_bounds__(Lay<I4>::kThreads, 1)
       }
     }
 
-    // reduce the four warps' partial sums and write this split's partials
-    aborted = tc::named_bar_or(bar, kWg, aborted || broken || *abort_flag != 0);
+    // reduce the eight warps' partial sums and write this split's partials; the decision is
+    // taken over both warpgroups at once, so either both or neither enter the barriers below
+    aborted = tc::named_bar_or(7, 2 * kWg, aborted || broken || *abort_flag != 0);
     if (!aborted) {
       const float ls0 = warp_sum(l0), ls1 = warp_sum(l1);
       if (lane == 0) lred[e] = make_float2(ls0, ls1);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        ored[(e * kHeads + 0) * kVHalf + lane * 4 + c] = acc0[c];
-        ored[(e * kHeads + 1) * kVHalf + lane * 4 + c] = acc1[c];
+        reinterpret_cast<float2*>(ored + (w8 * kHeads + 0) * kRank + lane * 8)[c] = acc0[c];
+        reinterpret_cast<float2*>(ored + (w8 * kHeads + 1) * kRank + lane * 8)[c] = acc1[c];
       }
-      tc::named_bar(bar, kWg);
-      for (int idx = ei; idx < kHeads * kVHalf; idx += kWg) {
-        const int j = idx / kVHalf, c = idx % kVHalf;
+      tc::named_bar(7, 2 * kWg);
+      const int t2 = threadIdx.x - 3 * kWg;   // 0..255
+#pragma unroll
+      for (int j = 0; j < kHeads; ++j) {
         float o = 0.f;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) o += ored[(k * kHeads + j) * kVHalf + c];
+        for (int k = 0; k < 8; ++k) o += ored[(k * kHeads + j) * kRank + t2];
         const int64_t bh = (int64_t)b * a.n_heads + head0 + j;
-        a.part_o[(bh * a.n_splits + split) * kRank + Y * kVHalf + c] = o;
+        a.part_o[(bh * a.n_splits + split) * kRank + t2] = o;
       }
       if (Y == 0 && ei < kHeads) {
         float L = 0.f;
