@@ -100,8 +100,18 @@ typedef struct palu_attn_desc {
   int max_batch;          /* largest batch any decode call will pass */
   int64_t max_tokens;     /* largest sequence length any decode call will see */
   int64_t max_position;   /* positions must lie in [0, max_position); 0 means max_tokens */
-  uint32_t flags;         /* reserved, must be 0 */
+  uint32_t flags;         /* 0, or PALU_FLAG_TEST_STALL (test builds of callers only) */
 } palu_attn_desc;
+
+/*
+ * Failure-detection test hook; the pages have no counterpart. With this flag the
+ * tensor-core RoPE kernel's H_v producer issues no loads, so the consumers' bounded
+ * waits give up (after 50 ms instead of the normal 1 s), every CTA drains its copies,
+ * frees its tensor memory and returns, and the next palu_attn_check reports
+ * PALU_ERR_TIMEOUT. Outputs of such a call are undefined. The other kernels ignore it
+ * (palu_decode_plan tells which kernel a call uses). Never set it in production.
+ */
+#define PALU_FLAG_TEST_STALL 0x80000000u
 
 /*
  * A latent cache, caller-owned device memory. With n_g = n_heads / group_size:

@@ -39,7 +39,7 @@ constexpr int kRowBytes = kRank * 2;           // 512
 constexpr int kHalfStage = kStageTok * kRowBytes;  // 32 KB (K or V)
 constexpr int kStageBytes = 2 * kHalfStage;    // 64 KB
 constexpr int kThreads = (kWarps + 1) * 32;
-constexpr uint64_t kWaitNs = 1000000000ull;
+constexpr uint64_t kWaitNs = 1000000000ull;   // 1 s per wait
 
 constexpr int kOffRing = 0;
 constexpr int kOffBar = kOffRing + kStages * kStageBytes;

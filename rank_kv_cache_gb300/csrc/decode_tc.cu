@@ -52,7 +52,7 @@ constexpr int kBChunk = kN * kKChunk * 2;        // 32 KB
 constexpr int kBBytes = kBChunk * kChunks;       // 128 KB
 constexpr int kWg = 128;                         // threads per warpgroup
 constexpr uint32_t kTmemCols = 512;              // two N=256 fp32 accumulators
-constexpr uint64_t kWaitNs = 1000000000ull;      // 1 s per wait
+
 constexpr float kTurnToRad = 1.4629180792671596e-09f;  // 2 pi / 2^32
 
 // Per-variant layout. I4 = int4 latents: the H_k tile arrives packed (16 KB) and a converter
@@ -180,6 +180,7 @@ __global__ void __launch_bounds__(Lay<I4>::kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const DecodeArgs& a = P.a;
+  const uint64_t kWaitNs = a.wait_ns;   // bound of every mbarrier wait (1 s; shorter in the stall test)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wg = threadIdx.x / kWg;
   const int hp = blockIdx.x % P.hp_count, split = blockIdx.x / P.hp_count;
@@ -390,7 +391,7 @@ __global__ void __launch_bounds__(Lay<I4>::kThreads, 1)
       }
     } else if (warp == 2) {
       // ---------------------------------------------------------- H_v producer
-      if (lane == 0 && n_tiles > 0) {
+      if (lane == 0 && n_tiles > 0 && !a.test_stall) {
         tc::tma_prefetch(&tm_hv);
         int issued = 0;
         bool ok = true;

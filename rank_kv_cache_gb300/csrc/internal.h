@@ -48,6 +48,10 @@ struct DecodeArgs {
   unsigned* counters;
   float* out;
   float* lse;
+  // failure-detection test hook (PALU_FLAG_TEST_STALL): the tensor-core kernel's H_v
+  // producer issues nothing; wait_ns bounds every mbarrier wait of that kernel
+  int test_stall;
+  uint64_t wait_ns;
 };
 
 // create-time set-up

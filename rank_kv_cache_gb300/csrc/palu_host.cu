@@ -31,7 +31,7 @@ palu_status_t check_desc(const palu_attn_desc* d) {
   if (d->n_heads <= 0 || d->group_size <= 0 || d->n_heads % d->group_size != 0) return PALU_ERR_INVALID_ARG;
   if (d->max_batch <= 0 || d->max_tokens <= 0 || d->max_position < 0) return PALU_ERR_INVALID_ARG;
   if (d->max_tokens > (int64_t)1 << 30 || d->max_position > (int64_t)1 << 30) return PALU_ERR_INVALID_ARG;
-  if (d->flags != 0) return PALU_ERR_INVALID_ARG;
+  if ((d->flags & ~PALU_FLAG_TEST_STALL) != 0) return PALU_ERR_INVALID_ARG;
   if (d->mode != PALU_MODE_ROPE && d->mode != PALU_MODE_ABSORBED) return PALU_ERR_INVALID_ARG;
   if ((unsigned)d->k_dtype > PALU_INT4 || (unsigned)d->v_dtype > PALU_INT4) return PALU_ERR_INVALID_ARG;
   if ((unsigned)d->bk_dtype > PALU_BF16 || (unsigned)d->q_dtype > PALU_BF16) return PALU_ERR_INVALID_ARG;
@@ -328,6 +328,8 @@ static void fill_args(const palu_attn* h, const palu_cache* cache, int batch, in
   a.part_ml = reinterpret_cast<float2*>(h->ws + h->L.part_ml);
   a.err = reinterpret_cast<ErrWord*>(h->ws + h->L.err);
   a.counters = reinterpret_cast<unsigned*>(h->ws + h->L.counters);  // the decode kernels merge the splits
+  a.test_stall = (d.flags & PALU_FLAG_TEST_STALL) ? 1 : 0;
+  a.wait_ns = a.test_stall ? 50000000ull : 1000000000ull;   // bound of every device wait
 }
 
 // Kernel choice and split-T plan: tensor-core rebuild (RoPE; fp16, bf16 and int4 latents),

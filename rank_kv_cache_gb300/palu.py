@@ -23,6 +23,7 @@ PALU_OK, PALU_ERR_INVALID_ARG, PALU_ERR_UNSUPPORTED, PALU_ERR_CUDA, PALU_ERR_DEV
 PALU_F32, PALU_F16, PALU_BF16, PALU_INT4 = range(4)
 PALU_MODE_ROPE, PALU_MODE_ABSORBED = 0, 1
 PALU_KERNEL_TC_ROPE, PALU_KERNEL_TMA_ABSORBED, PALU_KERNEL_SIMT = 1, 2, 3
+PALU_FLAG_TEST_STALL = 0x80000000
 
 DTYPES = {"f32": PALU_F32, "f16": PALU_F16, "bf16": PALU_BF16, "int4": PALU_INT4}
 MODES = {"rope": PALU_MODE_ROPE, "absorbed": PALU_MODE_ABSORBED}
@@ -185,11 +186,11 @@ def _require_contiguous(**tensors):
 
 
 def make_desc(*, n_heads, head_dim, group_size, rank_k, rank_v, latent_dtype, q_dtype, mode, rope_theta=10000.0,
-              max_batch=1, max_tokens=1, max_position=0) -> palu_attn_desc:
+              max_batch=1, max_tokens=1, max_position=0, flags=0) -> palu_attn_desc:
     k = DTYPES[latent_dtype]
     bk = PALU_F16 if k == PALU_INT4 else k
     return palu_attn_desc(PALU_ABI_VERSION, n_heads, head_dim, group_size, rank_k, rank_v, k, k, bk,
-                          DTYPES[q_dtype], MODES[mode], float(rope_theta), max_batch, max_tokens, max_position, 0)
+                          DTYPES[q_dtype], MODES[mode], float(rope_theta), max_batch, max_tokens, max_position, flags)
 
 
 class LatentCache:
@@ -218,12 +219,12 @@ class PaluAttention:
     """Owns one handle and its torch-allocated workspace."""
 
     def __init__(self, bk, *, n_heads, head_dim, group_size, rank_k, rank_v, latent_dtype, q_dtype, mode,
-                 rope_theta=10000.0, max_batch=1, max_tokens=1, max_position=0, stream=None):
+                 rope_theta=10000.0, max_batch=1, max_tokens=1, max_position=0, flags=0, stream=None):
         torch = _torch()
         self.desc = make_desc(n_heads=n_heads, head_dim=head_dim, group_size=group_size, rank_k=rank_k,
                               rank_v=rank_v, latent_dtype=latent_dtype, q_dtype=q_dtype, mode=mode,
                               rope_theta=rope_theta, max_batch=max_batch, max_tokens=max_tokens,
-                              max_position=max_position)
+                              max_position=max_position, flags=flags)
         st, nbytes = palu_attn_workspace_size(self.desc)
         check(st, "palu_attn_workspace_size")
         self.workspace = torch.empty(nbytes + 256, dtype=torch.uint8, device=bk.device)

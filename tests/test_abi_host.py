@@ -71,6 +71,13 @@ def test_bad_descriptor_rejected(field, value, status):
     assert st == status
 
 
+def test_only_the_test_stall_flag_is_accepted():
+    st, _ = P.palu_attn_workspace_size(_desc(flags=P.PALU_FLAG_TEST_STALL))
+    assert st == P.PALU_OK
+    st, _ = P.palu_attn_workspace_size(_desc(flags=P.PALU_FLAG_TEST_STALL | 2))
+    assert st == P.PALU_ERR_INVALID_ARG
+
+
 def test_null_arguments_rejected_without_gpu():
     d = _desc()
     assert P._lib.palu_attn_workspace_size(ctypes.byref(d), None) == P.PALU_ERR_INVALID_ARG

@@ -199,3 +199,45 @@ def test_kernel_choice_per_workload(cid, kernel):
     got, n_splits, launches = attn.plan(cfg.T, cfg.batch, cfg.T)
     assert got == getattr(P, "PALU_KERNEL_" + kernel)
     assert n_splits >= 1 and launches == (1 if kernel == "TC_ROPE" else 2)
+
+
+def test_bounded_wait_gives_up_and_reports_timeout():
+    # failure detection without a fault: with the test-stall flag the H_v producer of the
+    # tensor-core kernel issues nothing, every consumer wait gives up after its bound, the
+    # CTAs unwind, and the error word reports PALU_ERR_TIMEOUT; the context stays usable
+    import torch
+    from rank_kv_cache_gb300 import palu as P
+    cfg = gen.CONFIGS[2].with_(T=300, batch=2)
+    c = Case(cfg)
+    stall = P.PaluAttention(c.bk_t.to(c.dev), n_heads=cfg.n_heads, head_dim=cfg.head_dim,
+                            group_size=cfg.group_size, rank_k=cfg.rank, rank_v=cfg.rank, latent_dtype="f16",
+                            q_dtype=cfg.q_dtype, mode="rope", max_batch=cfg.batch, max_tokens=cfg.T,
+                            flags=P.PALU_FLAG_TEST_STALL)
+    assert stall.plan(cfg.T, cfg.batch, cfg.T)[0] == P.PALU_KERNEL_TC_ROPE
+    seq = torch.full((cfg.batch,), cfg.T, dtype=torch.int32, device=c.dev)
+    stall.decode(c.q_t.to(c.dev), c.cache, seq, max_seq_len=cfg.T)
+    torch.cuda.synchronize()
+    with pytest.raises(P.PaluError) as ei:
+        stall.check_device()
+    assert ei.value.status == P.PALU_ERR_TIMEOUT
+    stall.check_device()        # reading the error word cleared it
+    out, lse = c.run_gpu()      # the normal handle still decodes correctly afterwards
+    ref, lse_ref = c.run_oracle()
+    assert_close(out, ref, lse, lse_ref)
+
+
+def test_cache_saved_and_reloaded_decodes_identically():
+    # the library keeps no state between calls: a cache copied out to the host and back
+    # into fresh device buffers gives the same bits
+    import torch
+    from rank_kv_cache_gb300 import palu as P
+    cfg = gen.CONFIGS[5].with_(T=400, batch=2)
+    c = Case(cfg, seq_lens=[400, 123])
+    out1, lse1 = c.run_gpu()
+    saved = {k: getattr(c.cache, k).cpu() for k in ("hk", "hv", "k_scale", "v_scale")}
+    fresh = P.LatentCache(cfg.batch, c.capacity, cfg.n_groups, cfg.rank, cfg.rank, "int4", device=c.dev)
+    for k, v in saved.items():
+        getattr(fresh, k).copy_(v.to(c.dev))
+    c.cache = fresh
+    out2, lse2 = c.run_gpu()
+    assert np.array_equal(out1, out2) and np.array_equal(lse1, lse2)
