@@ -149,6 +149,52 @@ __device__ __forceinline__ uint4 int4x8_to_half8(uint32_t w) {
   return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
+// Fold the rotated query into B_k^T, in place, before the first MMA: for head j and rotation
+// pair k, rows a = 128 j + k and b = a + 64 of B_k^T become
+//   U = q_a B_a + q_b B_b   and   W = q_b B_a - q_a B_b,
+// so the MMA yields X_k = q_a k_a + q_b k_b and Y_k = q_b k_a - q_a k_b per token and the
+// rotated score is sum_k cos X_k + sin Y_k. Rows a and b share their swizzle phase (a = b mod 8),
+// so element m of both rows sits at the same offset in its row. Run by the 512 threads of the
+// score and softmax warpgroups (tf = 0..511), one 64-column chunk at a time as its TMA lands;
+// returns false if a wait gave up.
+__device__ __forceinline__ bool fold_b(uint8_t* b_smem, const float4* qs, uint64_t* bfull, uint64_t* bready, int tf,
+                                       int lane, volatile int* abort_flag, uint64_t wait_ns) {
+  bool ok = true;
+  for (int kc = 0; kc < kChunks; ++kc) {
+    if (ok && !tc::mbar_wait_bounded(&bfull[kc], 0, abort_flag, wait_ns)) ok = false;
+    if (ok) {
+      uint8_t* chunk = b_smem + kc * kBChunk;
+#pragma unroll
+      for (int rep = 0; rep < 2; ++rep) {
+        const int job = tf + rep * 4 * kWg;            // 0..1023: (head, pair, 16-byte chunk)
+        const int c = job & 7, k = (job >> 3) & (kHalf - 1), j = job >> 9;
+        const int ra = j * kDh + k;
+        const float4 q4 = qs[k];
+        const float qa = j ? q4.y : q4.x, qb = j ? q4.w : q4.z;
+        uint4* pa = reinterpret_cast<uint4*>(chunk + ra * 128 + ((c ^ (ra & 7)) << 4));
+        uint4* pb = reinterpret_cast<uint4*>(chunk + (ra + kHalf) * 128 + ((c ^ (ra & 7)) << 4));
+        uint4 va = *pa, vb = *pb;
+        __half2* ha = reinterpret_cast<__half2*>(&va);
+        __half2* hb = reinterpret_cast<__half2*>(&vb);
+#pragma unroll
+        for (int e2 = 0; e2 < 4; ++e2) {
+          const float2 ba = __half22float2(ha[e2]), bb = __half22float2(hb[e2]);
+          const float2 uu = make_float2(fmaf(qa, ba.x, qb * bb.x), fmaf(qa, ba.y, qb * bb.y));
+          const float2 ww = make_float2(fmaf(qb, ba.x, -qa * bb.x), fmaf(qb, ba.y, -qa * bb.y));
+          ha[e2] = __float22half2_rn(uu);
+          hb[e2] = __float22half2_rn(ww);
+        }
+        *pa = va;
+        *pb = vb;
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor cores
+    }
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(&bready[kc]);
+  }
+  return ok;
+}
+
 __device__ __forceinline__ int token_position(const DecodeArgs& a, int b, int t, bool valid) {
   int pos = t;
   if (valid && a.positions) pos = a.positions[(int64_t)b * a.capacity + t];
@@ -240,7 +286,7 @@ __global__ void __launch_bounds__(Lay<I4>::kThreads, 1)
       tc::mbar_init(&pempty[i], 4);   // converter warps
     }
     tc::mbar_init(mma_done, 1);
-    for (int i = 0; i < kChunks; ++i) tc::mbar_init(&bready[i], 8);  // eight softmax/PV warps
+    for (int i = 0; i < kChunks; ++i) tc::mbar_init(&bready[i], 16);  // score + softmax/PV warps
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
@@ -424,6 +470,7 @@ __global__ void __launch_bounds__(Lay<I4>::kThreads, 1)
     // ran on the integer codes and the token's key scale multiplies the score (RoPE and the
     // dot product are linear in the key).
     setmaxnreg_inc<LY::kRegsScore>();
+    if (FOLD && n_tiles > 0) fold_b(smem + LY::kOffB, qs, bfull, bready, threadIdx.x - kWg, lane, abort_flag, kWaitNs);
     const int X = wg - 1;
     const int quad = warp & 3;               // TMEM lane quadrant this warp may access
     const int row = quad * 32 + lane;
@@ -532,45 +579,7 @@ __global__ void __launch_bounds__(Lay<I4>::kThreads, 1)
     bool aborted = false;  // warpgroup-uniform: only ever set from a barrier-OR
     bool broken = false;   // this warp's own H_v wait gave up
     if (FOLD && n_tiles > 0) {  // (B_k is loaded only when the CTA has tokens)
-      // Fold the rotated query into B_k^T, in place, before the first MMA: for head j and
-      // rotation pair k, rows a = 128 j + k and b = a + 64 of B_k^T become
-      //   U = q_a B_a + q_b B_b   and   W = q_b B_a - q_a B_b,
-      // so the MMA yields X_k = q_a k_a + q_b k_b and Y_k = q_b k_a - q_a k_b per token and the
-      // rotated score is sum_k cos X_k + sin Y_k. Rows a and b share their swizzle phase (a = b
-      // mod 8), so element m of both rows sits at the same offset in its row.
-      const int t2 = threadIdx.x - 3 * kWg;  // 0..255
-      for (int kc = 0; kc < kChunks; ++kc) {
-        if (!tc::mbar_wait_bounded(&bfull[kc], 0, abort_flag, kWaitNs)) broken = true;
-        if (!broken) {
-          uint8_t* chunk = smem + LY::kOffB + kc * kBChunk;
-#pragma unroll
-          for (int rep = 0; rep < 4; ++rep) {
-            const int job = t2 + rep * 2 * kWg;          // 0..1023: (head, pair, 16-byte chunk)
-            const int c = job & 7, k = (job >> 3) & (kHalf - 1), j = job >> 9;
-            const int ra = j * kDh + k;
-            const float4 q4 = qs[k];
-            const float qa = j ? q4.y : q4.x, qb = j ? q4.w : q4.z;
-            uint4* pa = reinterpret_cast<uint4*>(chunk + ra * 128 + ((c ^ (ra & 7)) << 4));
-            uint4* pb = reinterpret_cast<uint4*>(chunk + (ra + kHalf) * 128 + ((c ^ (ra & 7)) << 4));
-            uint4 va = *pa, vb = *pb;
-            __half2* ha = reinterpret_cast<__half2*>(&va);
-            __half2* hb = reinterpret_cast<__half2*>(&vb);
-#pragma unroll
-            for (int e2 = 0; e2 < 4; ++e2) {
-              const float2 ba = __half22float2(ha[e2]), bb = __half22float2(hb[e2]);
-              const float2 uu = make_float2(fmaf(qa, ba.x, qb * bb.x), fmaf(qa, ba.y, qb * bb.y));
-              const float2 ww = make_float2(fmaf(qb, ba.x, -qa * bb.x), fmaf(qb, ba.y, -qa * bb.y));
-              ha[e2] = __float22half2_rn(uu);
-              hb[e2] = __float22half2_rn(ww);
-            }
-            *pa = va;
-            *pb = vb;
-          }
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor cores
-        }
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&bready[kc]);
-      }
+      if (!fold_b(smem + LY::kOffB, qs, bfull, bready, threadIdx.x - kWg, lane, abort_flag, kWaitNs)) broken = true;
     }
     float vs_next = 1.f;
     if constexpr (I4)

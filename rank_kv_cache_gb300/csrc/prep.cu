@@ -209,31 +209,54 @@ __device__ void append_row(const AppendSide& sd, int cache_dtype, int64_t capaci
   }
   const int64_t src_off = row * rank;
   const int64_t crow = ((int64_t)b * capacity + dst) * n_g + g;
+  // each lane owns `per` consecutive elements (rank / 32 = 2, 4 or 8); every load is issued
+  // before the first store, so a row costs one memory latency
+  const int per = rank / 32;
+  float h[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    if (k < per) h[k] = load_as_f32(sd.src, src_dtype, src_off + lane * per + k);
   if (cache_dtype != kINT4) {
-    for (int e = lane; e < rank; e += 32) {
-      const float v = load_as_f32(sd.src, src_dtype, src_off + e);
-      const int64_t o = crow * rank + e;
-      if (cache_dtype == kF32) static_cast<float*>(sd.cache)[o] = v;
-      else if (cache_dtype == kF16) static_cast<__half*>(sd.cache)[o] = __float2half_rn(v);
-      else static_cast<__nv_bfloat16*>(sd.cache)[o] = __float2bfloat16_rn(v);
+    const int64_t o = crow * rank + lane * per;
+    if (cache_dtype == kF32) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (k < per) static_cast<float*>(sd.cache)[o + k] = h[k];
+    } else if (per == 8) {
+      // one 16-byte store of eight 16-bit values (rows are 16-byte aligned)
+      uint32_t w[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (cache_dtype == kF16) {
+          const __half2 v = __floats2half2_rn(h[2 * j], h[2 * j + 1]);
+          w[j] = *reinterpret_cast<const uint32_t*>(&v);
+        } else {
+          const __nv_bfloat162 v = __floats2bfloat162_rn(h[2 * j], h[2 * j + 1]);
+          w[j] = *reinterpret_cast<const uint32_t*>(&v);
+        }
+      }
+      *reinterpret_cast<uint4*>(static_cast<uint16_t*>(sd.cache) + o) = make_uint4(w[0], w[1], w[2], w[3]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (k < per) {
+          if (cache_dtype == kF16) static_cast<__half*>(sd.cache)[o + k] = __float2half_rn(h[k]);
+          else static_cast<__nv_bfloat16*>(sd.cache)[o + k] = __float2bfloat16_rn(h[k]);
+        }
+      }
     }
     return;
   }
-  // int4: each lane owns `per` consecutive elements (rank / 32 = 2, 4 or 8)
-  const int per = rank / 32;
-  float h[8];
+  // int4: quantise the row with one scale
   float amax = 0.f;
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    if (k < per) {
-      h[k] = load_as_f32(sd.src, src_dtype, src_off + lane * per + k);
-      amax = fmaxf(amax, fabsf(h[k]));
-    }
-  }
+  for (int k = 0; k < 8; ++k)
+    if (k < per) amax = fmaxf(amax, fabsf(h[k]));
   amax = warp_max(amax);
   const __half sc = __float2half_rn(fminf(__fdiv_rn(amax, 7.0f), 65504.0f));
   const float sf = __half2float(sc);
   uint8_t* out = static_cast<uint8_t*>(sd.cache) + crow * (rank / 2) + lane * (per / 2);
+  uint32_t packed = 0;   // byte j = elements 2j (low nibble) and 2j + 1 (high nibble)
 #pragma unroll
   for (int k = 0; k < 8; k += 2) {
     if (k < per) {
@@ -242,8 +265,13 @@ __device__ void append_row(const AppendSide& sd, int cache_dtype, int64_t capaci
         c0 = int(fminf(fmaxf(rintf(__fdiv_rn(h[k], sf)), -7.f), 7.f));
         c1 = int(fminf(fmaxf(rintf(__fdiv_rn(h[k + 1], sf)), -7.f), 7.f));
       }
-      out[k / 2] = uint8_t((c0 & 0xF) | ((c1 & 0xF) << 4));
+      packed |= uint32_t((c0 & 0xF) | ((c1 & 0xF) << 4)) << (4 * k);
     }
+  }
+  if (per == 8) {
+    *reinterpret_cast<uint32_t*>(out) = packed;   // 4-byte aligned: rows are 128-byte multiples
+  } else {
+    for (int j = 0; j < per / 2; ++j) out[j] = uint8_t(packed >> (8 * j));
   }
   if (lane == 0) sd.scale[crow] = sc;
 }
