@@ -149,8 +149,9 @@ __device__ __forceinline__ uint4 int4x8_to_half8(uint32_t w) {
   return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
-// Fold the rotated query into B_k^T, in place, before the first MMA: for head j and rotation
-// pair k, rows a = 128 j + k and b = a + 64 of B_k^T become
+// Fold the rotated query into B_k^T, in place, before the first MMA. B_k^T holds the head pair
+// interleaved (row 2 d + j = dimension d of head j). For head j and rotation pair k, rows
+// a = 2 k + j (dimension k) and b = a + 128 (dimension k + 64) become
 //   U = q_a B_a + q_b B_b   and   W = q_b B_a - q_a B_b,
 // so the MMA yields X_k = q_a k_a + q_b k_b and Y_k = q_b k_a - q_a k_b per token and the
 // rotated score is sum_k cos X_k + sin Y_k. Rows a and b share their swizzle phase (a = b mod 8),
@@ -168,11 +169,11 @@ __device__ __forceinline__ bool fold_b(uint8_t* b_smem, const float4* qs, uint64
       for (int rep = 0; rep < 2; ++rep) {
         const int job = tf + rep * 4 * kWg;            // 0..1023: (head, pair, 16-byte chunk)
         const int c = job & 7, k = (job >> 3) & (kHalf - 1), j = job >> 9;
-        const int ra = j * kDh + k;
+        const int ra = 2 * k + j;
         const float4 q4 = qs[k];
         const float qa = j ? q4.y : q4.x, qb = j ? q4.w : q4.z;
         uint4* pa = reinterpret_cast<uint4*>(chunk + ra * 128 + ((c ^ (ra & 7)) << 4));
-        uint4* pb = reinterpret_cast<uint4*>(chunk + (ra + kHalf) * 128 + ((c ^ (ra & 7)) << 4));
+        uint4* pb = reinterpret_cast<uint4*>(chunk + (ra + kDh) * 128 + ((c ^ (ra & 7)) << 4));
         uint4 va = *pa, vb = *pb;
         __half2* ha = reinterpret_cast<__half2*>(&va);
         __half2* hb = reinterpret_cast<__half2*>(&vb);
@@ -497,15 +498,17 @@ __global__ void __launch_bounds__(Lay<I4>::kThreads, 1)
       if (tc::named_bar_or(1 + X, kWg, !got)) break;  // one decision for the warpgroup
       tc::tc_fence_after();
 
-      float s0a = 0.f, s0b = 0.f, s1a = 0.f, s1b = 0.f;
+      // accumulator columns: 2 d + j = dimension d of head j, so (head 0, head 1) of a dimension
+      // are adjacent and one packed f32x2 instruction updates both heads
+      float2 sa = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f);
       const uint32_t tbase = tmem_base + (uint32_t(quad * 32) << 16) + buf * kN;
 #pragma unroll 1
       for (int a0 = 32 * X; a0 < 32 * X + 32; a0 += 16) {
-        // issue the four TMEM loads of this chunk (pairs a0..a0+15 of both heads), compute
-        // the chunk's cos/sin while they are in flight, then wait
-        uint32_t k0[32], k1[32];
-        tc::tmem_ld16x2_nowait(tbase + a0, tbase + kHalf + a0, k0);
-        tc::tmem_ld16x2_nowait(tbase + kDh + a0, tbase + kDh + kHalf + a0, k1);
+        // issue the four TMEM loads of this chunk (dimensions a0..a0+15 and a0+64..a0+79 of
+        // both heads), compute the chunk's cos/sin while they are in flight, then wait
+        uint32_t ka[32], kb[32];
+        tc::tmem_ld16x2_nowait(tbase + 2 * a0, tbase + 2 * a0 + 16, ka);
+        tc::tmem_ld16x2_nowait(tbase + kDh + 2 * a0, tbase + kDh + 2 * a0 + 16, kb);
         float cs[16], sn[16];
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
@@ -514,38 +517,28 @@ __global__ void __launch_bounds__(Lay<I4>::kThreads, 1)
           __sincosf(float(int32_t(top)) * kTurnToRad, &sn[u], &cs[u]);
         }
         tc::tmem_ld_wait();
-        if constexpr (FOLD) {
-          // the MMA produced X_k = q_a k_a + q_b k_b and Y_k = q_b k_a - q_a k_b directly
 #pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            const float x0 = __uint_as_float(k0[u]), y0 = __uint_as_float(k0[16 + u]);
-            const float x1 = __uint_as_float(k1[u]), y1 = __uint_as_float(k1[16 + u]);
-            if (u & 1) {
-              s0b = fmaf(sn[u], y0, fmaf(cs[u], x0, s0b));
-              s1b = fmaf(sn[u], y1, fmaf(cs[u], x1, s1b));
-            } else {
-              s0a = fmaf(sn[u], y0, fmaf(cs[u], x0, s0a));
-              s1a = fmaf(sn[u], y1, fmaf(cs[u], x1, s1a));
-            }
-          }
-        } else {
-#pragma unroll
-          for (int u = 0; u < 16; ++u) {
+        for (int u = 0; u < 16; ++u) {
+          const float2 c2 = make_float2(cs[u], cs[u]), s2 = make_float2(sn[u], sn[u]);
+          const float2 xa = make_float2(__uint_as_float(ka[2 * u]), __uint_as_float(ka[2 * u + 1]));
+          const float2 xb = make_float2(__uint_as_float(kb[2 * u]), __uint_as_float(kb[2 * u + 1]));
+          float2& acc = (u & 1) ? sb : sa;
+          if constexpr (FOLD) {
+            // the MMA produced X_k (xa) and Y_k (xb) directly
+            acc = __ffma2_rn(c2, xa, acc);
+            acc = __ffma2_rn(s2, xb, acc);
+          } else {
+            // c (q_a k_a + q_b k_b) + s (q_b k_a - q_a k_b) = k_a (c q_a + s q_b) + k_b (c q_b - s q_a)
             const float4 q4 = qs[a0 + u];     // (qa0, qa1, qb0, qb1)
-            const float ka0 = __uint_as_float(k0[u]), kb0 = __uint_as_float(k0[16 + u]);
-            const float ka1 = __uint_as_float(k1[u]), kb1 = __uint_as_float(k1[16 + u]);
-            const float t0v = fmaf(q4.x, ka0, q4.z * kb0), v0 = fmaf(q4.z, ka0, -q4.x * kb0);
-            const float t1v = fmaf(q4.y, ka1, q4.w * kb1), v1 = fmaf(q4.w, ka1, -q4.y * kb1);
-            if (u & 1) {
-              s0b = fmaf(sn[u], v0, fmaf(cs[u], t0v, s0b));
-              s1b = fmaf(sn[u], v1, fmaf(cs[u], t1v, s1b));
-            } else {
-              s0a = fmaf(sn[u], v0, fmaf(cs[u], t0v, s0a));
-              s1a = fmaf(sn[u], v1, fmaf(cs[u], t1v, s1a));
-            }
+            const float2 qa = make_float2(q4.x, q4.y), qb = make_float2(q4.z, q4.w);
+            const float2 al = __ffma2_rn(s2, qb, __fmul2_rn(c2, qa));
+            const float2 be = __ffma2_rn(make_float2(-sn[u], -sn[u]), qa, __fmul2_rn(c2, qb));
+            acc = __ffma2_rn(xa, al, acc);
+            acc = __ffma2_rn(xb, be, acc);
           }
         }
       }
+      const float s0a = sa.x, s0b = sb.x, s1a = sa.y, s1b = sb.y;
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&tempty[buf]);

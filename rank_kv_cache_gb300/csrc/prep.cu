@@ -41,8 +41,12 @@ cudaError_t launch_rope_table(float2* tab, uint64_t* phase, int64_t max_pos, int
 // B_k copies: dst = B_k as given ([n_g][rk][cols]); dst_t = its per-group transpose
 // [n_g][cols][rk] in the MMA operand type (the K-major B operand of the rebuild GEMM).
 // ---------------------------------------------------------------------------
+// dst_t = B_k^T as the tensor-core kernel's K-major operand, [n_g][s * d_h][r]. With an even
+// group size the rows of each head pair are interleaved by head (row 2 d + (j & 1) of pair j / 2
+// holds dimension d of head j), so the MMA writes the two heads' values of a dimension into
+// adjacent accumulator columns and the epilogue updates both heads with one packed instruction.
 __global__ void copy_bk_kernel(const void* src, int bk_dtype, void* dst, void* dst_t, int mma_dtype, int n_g,
-                               int rk, int cols) {
+                               int rk, int cols, int dh) {
   const int64_t n = (int64_t)n_g * rk * cols;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
     const int c = int(i % cols);
@@ -54,7 +58,9 @@ __global__ void copy_bk_kernel(const void* src, int bk_dtype, void* dst, void* d
     else static_cast<uint16_t*>(dst)[i] = static_cast<const uint16_t*>(src)[i];
     if (dst_t) {
       const float v = load_as_f32(src, bk_dtype, i);
-      const int64_t o = ((int64_t)g * cols + c) * rk + m;
+      const int j = c / dh, d = c % dh;
+      const int ct = ((cols / dh) % 2 == 0) ? (j / 2) * 2 * dh + 2 * d + (j & 1) : c;
+      const int64_t o = ((int64_t)g * cols + ct) * rk + m;
       if (mma_dtype == kBF16) static_cast<__nv_bfloat16*>(dst_t)[o] = __float2bfloat16_rn(v);
       else static_cast<__half*>(dst_t)[o] = __float2half_rn(v);
     }
@@ -62,10 +68,10 @@ __global__ void copy_bk_kernel(const void* src, int bk_dtype, void* dst, void* d
 }
 
 cudaError_t launch_copy_bk(const void* src, int bk_dtype, void* dst, void* dst_t, int mma_dtype, int n_g, int rk,
-                           int cols, cudaStream_t st) {
+                           int cols, int dh, cudaStream_t st) {
   const int64_t n = (int64_t)n_g * rk * cols;
   const int blocks = int((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
-  copy_bk_kernel<<<blocks, 256, 0, st>>>(src, bk_dtype, dst, dst_t, mma_dtype, n_g, rk, cols);
+  copy_bk_kernel<<<blocks, 256, 0, st>>>(src, bk_dtype, dst, dst_t, mma_dtype, n_g, rk, cols, dh);
   return cudaGetLastError();
 }
 
