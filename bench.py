@@ -207,6 +207,22 @@ def _dist():
     return world, rank, local
 
 
+def max_over_ranks(x, dist=None, device="cpu"):
+    """The largest value of x across the ranks (x itself without a process group)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput_gbs(world, bytes_per_rank_step, ms_per_step):
+    """Whole-job GB/s of independent replicas: every rank moves bytes_per_rank_step per step and the
+    step takes as long as the slowest rank (weak scaling)."""
+    return world * bytes_per_rank_step / 1e9 / (ms_per_step / 1e3)
+
+
 class GpuWorkload:
     """Device-resident workload: cache filled through the append kernel, per-step inputs."""
 
@@ -300,11 +316,7 @@ def run_gpu(args, cfg, name):
     P.check(st)
     P.palu_attn_trace_enable(wl.attn.handle, 0)
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    tot_ms = sum(step_ms)
-    if dist:
-        t = torch.tensor([tot_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        tot_ms = float(t.item())
+    tot_ms = max_over_ranks(sum(step_ms), dist, dev)
     ms_per_step = tot_ms / K
     kernel_ms = tr_ms / max(n_tr, 1)
     wl.attn.check_device()
@@ -331,20 +343,15 @@ def run_gpu(args, cfg, name):
         b.record()
         b.synchronize()
         e2e_ms.append(a.elapsed_time(b))
-    e2e_step = statistics.mean(e2e_ms)
-    if dist:
-        t = torch.tensor([e2e_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_step = float(t.item())
+    e2e_step = max_over_ranks(statistics.mean(e2e_ms), dist, dev)
 
     peaks, peaks_src = load_peaks()
     roof = roofline_for(cfg, work, kernel_ms, peaks, peaks_src, long_step=ms_per_step > 10.0)
     roof["kernel"] = wl.kernel_name
     roof["traffic"] = recorded_traffic(name, wl.kernel_name, cfg)
-    gb = work["decode_bytes"] / 1e9
     result = {
         "metric": METRIC,
-        "value": round(world * gb / (ms_per_step / 1e3), 2),
+        "value": round(job_throughput_gbs(world, work["decode_bytes"], ms_per_step), 2),
         "unit": "GB/s",
         "n_gpus": world,
         "steps": K,
@@ -363,11 +370,12 @@ def run_gpu(args, cfg, name):
                    "l2": "flushed (512 MB write) before every timed step",
                    "bytes_per_step": work["decode_bytes"], "flops_per_step": work["flops"],
                    "dense_fp16_kv_bytes_per_step": work["dense_fp16_kv_bytes"]},
-        "dense_equiv_gbs": round(world * work["dense_fp16_kv_bytes"] / 1e9 / (ms_per_step / 1e3), 1),
+        "dense_equiv_gbs": round(job_throughput_gbs(world, work["dense_fp16_kv_bytes"], ms_per_step), 1),
         "roofline": roof,
         "kernel_us": round(kernel_ms * 1e3, 2),
         "kernel_launches_traced": n_tr,
-        "e2e": {"value": round(world * gb / (e2e_step / 1e3), 2), "unit": "GB/s", "ms_per_step": round(e2e_step, 6),
+        "e2e": {"value": round(job_throughput_gbs(world, work["decode_bytes"], e2e_step), 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_step, 6),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke},
         "gpu_launches": wl.launches_per_step * K,
         "clocks": clk.summary(),
