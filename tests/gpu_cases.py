@@ -28,7 +28,7 @@ class Case:
     """One workload on the GPU plus everything the oracle needs to check it."""
 
     def __init__(self, cfg: gen.Config, *, seq_lens=None, positions=None, q_pos=None, q_scale=1.0,
-                 capacity=None, max_position=0, fill="append"):
+                 capacity=None, max_position=0, fill="append", q_dtype=None):
         import torch
         from rank_kv_cache_gb300 import palu as P
         self.cfg = cfg
@@ -41,11 +41,12 @@ class Case:
         self.q_pos = None if q_pos is None else np.ascontiguousarray(q_pos, dtype=np.int32)
         self.capacity = capacity or T
         lat = cfg.latent_dtype
-        self.q_t = gen.storage_round(inp["q"], cfg.q_dtype)
+        self.q_dtype = q_dtype or cfg.q_dtype
+        self.q_t = gen.storage_round(inp["q"], self.q_dtype)
         self.bk_t = gen.storage_round(inp["bk"], cfg.bk_dtype)
         self.attn = P.PaluAttention(self.bk_t.to(dev), n_heads=cfg.n_heads, head_dim=cfg.head_dim,
                                     group_size=cfg.group_size, rank_k=cfg.rank, rank_v=cfg.rank, latent_dtype=lat,
-                                    q_dtype=cfg.q_dtype, mode=cfg.mode, rope_theta=cfg.theta, max_batch=B,
+                                    q_dtype=self.q_dtype, mode=cfg.mode, rope_theta=cfg.theta, max_batch=B,
                                     max_tokens=self.capacity, max_position=max_position)
         self.cache = P.LatentCache(B, self.capacity, cfg.n_groups, cfg.rank, cfg.rank, lat, device=dev)
         if lat == "int4":

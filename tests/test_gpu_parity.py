@@ -58,6 +58,31 @@ def test_absorbed_fp16_ragged():
     assert_close(out, ref, lse, lse_ref)
 
 
+def test_absorbed_bf16_ragged():
+    cfg = gen.CONFIGS[4].with_(T=1000, batch=3, latent_dtype="bf16")
+    c = Case(cfg, seq_lens=[1000, 1, 517])
+    out, lse = c.run_gpu()
+    ref, lse_ref = c.run_oracle()
+    assert_close(out, ref, lse, lse_ref)
+
+
+def test_absorbed_int4_on_cuda_cores():
+    cfg = gen.CONFIGS[4].with_(T=300, batch=2, latent_dtype="int4")
+    c = Case(cfg, seq_lens=[300, 77])
+    out, lse = c.run_gpu()
+    ref, lse_ref = c.run_oracle()
+    assert_close(out, ref, lse, lse_ref)
+
+
+@pytest.mark.parametrize("cid", [2, 4])
+def test_float32_query(cid):
+    cfg = gen.CONFIGS[cid].with_(T=500, batch=2)
+    c = Case(cfg, seq_lens=[500, 250], q_dtype="f32")
+    out, lse = c.run_gpu()
+    ref, lse_ref = c.run_oracle()
+    assert_close(out, ref, lse, lse_ref)
+
+
 def test_peaked_softmax_stress():
     cfg = gen.CONFIGS[2].with_(T=512, batch=1)
     c = Case(cfg, q_scale=8.0)
