@@ -128,19 +128,18 @@ __device__ __forceinline__ void vt8_to_float2x4(const uint4& u, float2* f, __nv_
 }
 
 // eight signed 4-bit codes of a 32-bit word (element 2j = low nibble of byte j) as eight
-// exact fp16 values: each nibble biased by 8 is placed under the fp16 exponent of 1024
-// (0x64xx), and 1032 is subtracted.
+// exact fp16 values, in the order [0, 2, 4, 6, 1, 3, 5, 7] (B_k^T is stored with its ranks
+// permuted alike): each nibble biased by 8 is placed under the fp16 exponent of 1024 (0x64xx),
+// and 1032 is subtracted.
 __device__ __forceinline__ uint4 int4x8_to_half8(uint32_t w) {
-  const uint32_t lo = (w & 0x0F0F0F0Fu) ^ 0x08080808u;
-  const uint32_t hi = ((w >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
-  const uint32_t i01 = __byte_perm(lo, hi, 0x5140);   // lo0 hi0 lo1 hi1
-  const uint32_t i23 = __byte_perm(lo, hi, 0x7362);   // lo2 hi2 lo3 hi3
+  const uint32_t lo = (w & 0x0F0F0F0Fu) ^ 0x08080808u;          // elements 0, 2, 4, 6
+  const uint32_t hi = ((w >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;   // elements 1, 3, 5, 7
   const __half2 bias = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));  // 1032
   uint32_t r[4];
-  r[0] = __byte_perm(i01, 0x64646464u, 0x4140);
-  r[1] = __byte_perm(i01, 0x64646464u, 0x4342);
-  r[2] = __byte_perm(i23, 0x64646464u, 0x4140);
-  r[3] = __byte_perm(i23, 0x64646464u, 0x4342);
+  r[0] = __byte_perm(lo, 0x64646464u, 0x4140);
+  r[1] = __byte_perm(lo, 0x64646464u, 0x4342);
+  r[2] = __byte_perm(hi, 0x64646464u, 0x4140);
+  r[3] = __byte_perm(hi, 0x64646464u, 0x4342);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&r[i]), bias);

@@ -57,7 +57,7 @@ struct DecodeArgs {
 // create-time set-up
 cudaError_t launch_rope_table(float2* tab, uint64_t* phase, int64_t max_pos, int dh, double theta, cudaStream_t st);
 cudaError_t launch_copy_bk(const void* src, int bk_dtype, void* dst, void* dst_t, int mma_dtype, int n_g,
-                           int rk, int cols, int dh, cudaStream_t st);
+                           int rk, int cols, int dh, int perm8, cudaStream_t st);
 
 // per-call kernels
 cudaError_t launch_qprep(int mode, const void* q, int q_dtype, const DecodeArgs& a, const int32_t* q_pos,

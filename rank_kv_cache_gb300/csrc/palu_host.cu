@@ -188,7 +188,7 @@ palu_status_t palu_attn_create(const palu_attn_desc* desc, const void* B_k, void
   void* bkt = (desc->mode == PALU_MODE_ROPE && desc->k_dtype != PALU_F32) ? h->ws + L.bkt : nullptr;
   if (e == cudaSuccess)
     e = launch_copy_bk(B_k, to_dt(desc->bk_dtype), h->ws + L.bk, bkt, h->mma_dtype, h->n_g, desc->rank_k, cols,
-                       desc->head_dim, s);
+                       desc->head_dim, desc->k_dtype == PALU_INT4 ? 1 : 0, s);
   if (e == cudaSuccess && desc->mode == PALU_MODE_ROPE)
     e = launch_rope_table(reinterpret_cast<float2*>(h->ws + L.rope), reinterpret_cast<uint64_t*>(h->ws + L.phase),
                           L.max_pos, desc->head_dim, desc->rope_theta, s);

@@ -45,8 +45,11 @@ cudaError_t launch_rope_table(float2* tab, uint64_t* phase, int64_t max_pos, int
 // group size the rows of each head pair are interleaved by head (row 2 d + (j & 1) of pair j / 2
 // holds dimension d of head j), so the MMA writes the two heads' values of a dimension into
 // adjacent accumulator columns and the epilogue updates both heads with one packed instruction.
+// perm8 (int4 caches): within each group of eight ranks, position p holds rank [0,2,4,6,1,3,5,7][p],
+// the order in which the int4 converter emits a packed word's codes; permuting K in both MMA
+// operands alike leaves the product unchanged.
 __global__ void copy_bk_kernel(const void* src, int bk_dtype, void* dst, void* dst_t, int mma_dtype, int n_g,
-                               int rk, int cols, int dh) {
+                               int rk, int cols, int dh, int perm8) {
   const int64_t n = (int64_t)n_g * rk * cols;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
     const int c = int(i % cols);
@@ -60,7 +63,8 @@ __global__ void copy_bk_kernel(const void* src, int bk_dtype, void* dst, void* d
       const float v = load_as_f32(src, bk_dtype, i);
       const int j = c / dh, d = c % dh;
       const int ct = ((cols / dh) % 2 == 0) ? (j / 2) * 2 * dh + 2 * d + (j & 1) : c;
-      const int64_t o = ((int64_t)g * cols + ct) * rk + m;
+      const int mt = perm8 ? (m & ~7) | ((m & 1) << 2) | ((m & 7) >> 1) : m;
+      const int64_t o = ((int64_t)g * cols + ct) * rk + mt;
       if (mma_dtype == kBF16) static_cast<__nv_bfloat16*>(dst_t)[o] = __float2bfloat16_rn(v);
       else static_cast<__half*>(dst_t)[o] = __float2half_rn(v);
     }
@@ -68,10 +72,10 @@ __global__ void copy_bk_kernel(const void* src, int bk_dtype, void* dst, void* d
 }
 
 cudaError_t launch_copy_bk(const void* src, int bk_dtype, void* dst, void* dst_t, int mma_dtype, int n_g, int rk,
-                           int cols, int dh, cudaStream_t st) {
+                           int cols, int dh, int perm8, cudaStream_t st) {
   const int64_t n = (int64_t)n_g * rk * cols;
   const int blocks = int((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
-  copy_bk_kernel<<<blocks, 256, 0, st>>>(src, bk_dtype, dst, dst_t, mma_dtype, n_g, rk, cols, dh);
+  copy_bk_kernel<<<blocks, 256, 0, st>>>(src, bk_dtype, dst, dst_t, mma_dtype, n_g, rk, cols, dh, perm8);
   return cudaGetLastError();
 }
 
