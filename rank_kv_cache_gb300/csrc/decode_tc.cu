@@ -289,6 +289,29 @@ __global__ void __launch_bounds__(Lay<I4>::kThreads, 1)
     for (int i = 0; i < kChunks; ++i) tc::mbar_init(&bready[i], 16);  // score + softmax/PV warps
     *abort_flag = 0;
     tc::fence_barrier_init();
+    if (n_tiles > 0) {
+      // start B_k^T and the first operand tiles now, so their latency overlaps the query
+      // rotation and the TMEM allocation (this thread is the producer; the rings are empty)
+      tc::tma_prefetch(&tm_hk);
+      tc::tma_prefetch(&tm_b);
+      const int brow = g * (a.s * kDh) + hp * kN;
+      for (int kc = 0; kc < kChunks; ++kc) {
+        tc::mbar_arrive_expect_tx(&bfull[kc], kBChunk);
+        tc::tma_load_2d(smem + LY::kOffB + kc * kBChunk, &tm_b, &bfull[kc], kc * kKChunk, brow);
+      }
+      if constexpr (I4) {
+        for (int it = 0; it < min(kPStages, n_tiles); ++it) {
+          tc::mbar_arrive_expect_tx(&pfull[it], LY::kPStage);
+          tc::tma_load_3d(smem + LY::kOffPk + it * LY::kPStage, &tm_hk, &pfull[it], 0, g, row0 + t_begin + it * kTile);
+        }
+      } else {
+        for (int ci = 0; ci < min(kStages, kChunks * n_tiles); ++ci) {
+          tc::mbar_arrive_expect_tx(&fullA[ci], kAStage);
+          tc::tma_load_3d(smem + LY::kOffA + ci * kAStage, &tm_hk, &fullA[ci], (ci % kChunks) * kKChunk, g,
+                          row0 + t_begin + (ci / kChunks) * kTile);
+        }
+      }
+    }
   }
   if (warp == 1) {
     tc::tmem_alloc(tmem_slot, kTmemCols);
@@ -325,18 +348,12 @@ __global__ void __launch_bounds__(Lay<I4>::kThreads, 1)
     if (warp == 0) {
       // ---------------------------------------------------------- H_k / B producer
       if (lane == 0 && n_tiles > 0) {
-        tc::tma_prefetch(&tm_hk);
-        tc::tma_prefetch(&tm_b);
-        const int brow = g * (a.s * kDh) + hp * kN;
-        for (int kc = 0; kc < kChunks; ++kc) {
-          tc::mbar_arrive_expect_tx(&bfull[kc], kBChunk);
-          tc::tma_load_2d(smem + LY::kOffB + kc * kBChunk, &tm_b, &bfull[kc], kc * kKChunk, brow);
-        }
+        // B_k^T and the first ring fills were issued in the prologue
         bool ok = true;
-        int issued = 0;
         if constexpr (I4) {
           // whole packed tiles (128 tokens x 128 bytes) into the staging ring
-          for (int it = 0; it < n_tiles && ok; ++it) {
+          int issued = min(kPStages, n_tiles);
+          for (int it = issued; it < n_tiles && ok; ++it) {
             const int ps = it % kPStages;
             if (!tc::mbar_wait_bounded(&pempty[ps], ((it / kPStages) & 1) ^ 1, abort_flag, kWaitNs)) {
               ok = false;
@@ -352,34 +369,25 @@ __global__ void __launch_bounds__(Lay<I4>::kThreads, 1)
               tc::mbar_wait_bounded(&pfull[it % kPStages], (it / kPStages) & 1, &quiet, kWaitNs / 10);
           }
         } else {
-          int stage = 0;
-          uint32_t round = 0;
-          for (int it = 0; it < n_tiles && ok; ++it) {
-            const int t0 = t_begin + it * kTile;
-            for (int kc = 0; kc < kChunks; ++kc) {
-              if (!tc::mbar_wait_bounded(&emptyA[stage], (round & 1) ^ 1, abort_flag, kWaitNs)) {
-                ok = false;
-                break;
-              }
-              tc::mbar_arrive_expect_tx(&fullA[stage], kAStage);
-              tc::tma_load_3d(smem + LY::kOffA + stage * kAStage, &tm_hk, &fullA[stage], kc * kKChunk, g, row0 + t0);
-              ++issued;
-              if (++stage == kStages) {
-                stage = 0;
-                ++round;
-              }
+          // operand chunk ci = (tile ci / 4, 64-column chunk ci % 4) goes to stage ci % kStages
+          int issued = min(kStages, kChunks * n_tiles);
+          for (int ci = issued; ci < kChunks * n_tiles && ok; ++ci) {
+            const int stage = ci % kStages;
+            const uint32_t round = uint32_t(ci / kStages);
+            if (!tc::mbar_wait_bounded(&emptyA[stage], (round & 1) ^ 1, abort_flag, kWaitNs)) {
+              ok = false;
+              break;
             }
+            tc::mbar_arrive_expect_tx(&fullA[stage], kAStage);
+            tc::tma_load_3d(smem + LY::kOffA + stage * kAStage, &tm_hk, &fullA[stage], (ci % kChunks) * kKChunk, g,
+                            row0 + t_begin + (ci / kChunks) * kTile);
+            ++issued;
           }
           if (!ok) {
             // drain the copies still in flight before the CTA may exit
             volatile int quiet = 0;
-            for (int k = 0, s = stage, r = (int)round; k < (issued < kStages ? issued : kStages); ++k) {
-              if (--s < 0) {
-                s = kStages - 1;
-                --r;
-              }
-              tc::mbar_wait_bounded(&fullA[s], uint32_t(r) & 1, &quiet, kWaitNs / 10);
-            }
+            for (int ci = (issued > kStages ? issued - kStages : 0); ci < issued; ++ci)
+              tc::mbar_wait_bounded(&fullA[ci % kStages], uint32_t(ci / kStages) & 1, &quiet, kWaitNs / 10);
           }
         }
         if (!ok) {
