@@ -82,9 +82,11 @@ int to_dt(palu_dtype_t t) { return (int)t; }
 
 // Split-T plan. `slots` CTAs run at once; each unit (one CTA's share of a group) is cut
 // into `splits` ranges of `tps` tiles. Picks the split count with the smallest estimated
-// time waves * (tps + 1), where the +1 stands for a CTA's fixed cost (operand load,
-// partial write), which also keeps splits from growing without need.
-void plan_splits(int64_t tiles, int64_t units, int64_t slots, int64_t max_splits, int* n_splits, int* tps_out) {
+// time waves * (tps + fixed), where `fixed` is a CTA's fixed cost in tiles (prologue operand
+// loads, pipeline fill and drain, partial write and merge), which also keeps splits from
+// growing without need.
+void plan_splits(int64_t tiles, int64_t units, int64_t slots, int64_t max_splits, int fixed, int* n_splits,
+                 int* tps_out) {
   int64_t cap = tiles < max_splits ? tiles : max_splits;
   if (cap < 1) cap = 1;
   double best = 1e300;
@@ -94,7 +96,7 @@ void plan_splits(int64_t tiles, int64_t units, int64_t slots, int64_t max_splits
     const int64_t s2 = (tiles + tps - 1) / tps;
     if (s2 != s) continue;  // same plan as a smaller split count
     const int64_t waves = (units * s2 + slots - 1) / slots;
-    const double est = double(waves) * double(tps + 1);
+    const double est = double(waves) * double(tps + fixed);
     if (est < best - 1e-9) {
       best = est;
       best_s = s2;
@@ -346,7 +348,10 @@ static int plan_decode(const palu_attn* h, DecodeArgs& a) {
                                                         : kSimtTile;
   const int64_t tiles = a.max_seq_len > 0 ? (a.max_seq_len + tile - 1) / tile : 1;
   const int64_t units = (int64_t)a.batch * h->n_g * (kernel == PALU_KERNEL_TC_ROPE ? tc_ctas_per_group(a) : 1);
-  plan_splits(tiles, units, kernel == PALU_KERNEL_SIMT ? 2 * h->sm_count : h->sm_count, h->L.max_splits,
+  // CTA fixed costs in tiles, as measured on GB300 at the 32K-64K workloads: about four
+  // 128-token tiles for the tensor-core kernel, eight 64-token stages for the absorbed stream
+  const int fixed = kernel == PALU_KERNEL_TC_ROPE ? 4 : kernel == PALU_KERNEL_TMA_ABSORBED ? 8 : 1;
+  plan_splits(tiles, units, kernel == PALU_KERNEL_SIMT ? 2 * h->sm_count : h->sm_count, h->L.max_splits, fixed,
               &a.n_splits, &a.tiles_per_split);
   return kernel;
 }
