@@ -114,12 +114,21 @@ COMMON_SOURCES = ("split_merge.cuh", "internal.h", "common.cuh")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 
 
+def _code_only(text):
+    """Source text without comments and blank-space differences (what the compiler sees)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash(kernel):
-    """Hash of the source files a decode kernel is compiled from (first 16 hex digits)."""
+    """Hash of the code (comments and layout ignored) of the files a decode kernel is compiled
+    from, first 16 hex digits."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES[kernel] + COMMON_SOURCES:
-        with open(os.path.join(CSRC, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(CSRC, f), encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -6,20 +6,26 @@
 // applied to the rebuilt keys and they are dotted with the query; intermediates
 // never leave the chip. Here, per CTA:
 //   * one (batch row b, group g, head pair hp, T-split) unit; the head pair's
-//     slice of B_k^T (256 rows x r, K-major) stays in shared memory;
+//     slice of B_k^T (256 rows x r, K-major, the two heads' rows interleaved so a
+//     dimension's two heads land in adjacent accumulator columns) stays in shared
+//     memory;
+//   * fp16 / int4 operands: the rotated query is folded into that slice once, so the
+//     MMA yields q_a k_a + q_b k_b and q_b k_a - q_a k_b per rotation pair directly;
+//     bf16 operands rebuild K exactly and apply the query in the epilogue;
 //   * warp 0 streams 128-token x 64-rank chunks of H_k,g by TMA (128-byte swizzle)
-//     through a 3-stage ring; warp 2 streams 16-token chunks of H_v,g by TMA
-//     through a 5-slot ring;
+//     through a 3-stage ring (int4: packed tiles, expanded to exact fp16 codes by a
+//     converter warpgroup); warp 2 streams H_v,g chunks by TMA through a ring;
 //   * warp 1 issues tcgen05.mma (M=128 tokens, N=256 = 2 heads x d_h, K=r) into
 //     one of two TMEM accumulators;
 //   * two score warpgroups (one token row per thread, read with tcgen05.ld; each
-//     takes half of the 64 rotation pairs) rotate every rebuilt key pair at the
-//     token's position and dot it with the rotated query, leaving partial scores
-//     of the tile in a double-buffered slot in shared memory;
+//     takes half of the 64 rotation pairs) apply the rotation at the token's position
+//     with packed f32x2 FMAs for both heads, leaving partial scores of the tile in a
+//     double-buffered slot in shared memory;
 //   * two softmax warpgroups run the same online softmax (base 2) on the previous
-//     tile's scores and each accumulates p H_v for half of the value-latent
-//     columns on CUDA cores, so scoring and p H_v of consecutive tiles overlap;
-//     the T-split partials go to the merge kernel.
+//     tile's scores; for p H_v each lane owns 8 of the 256 value columns and the
+//     warps share out the tokens (fp16/bf16: packed FMAs; int4: dp2a on the raw codes
+//     with 15-bit weights), so scoring and p H_v of consecutive tiles overlap;
+//   * the last CTA of a unit merges the T-split partials, so a decode is one launch;
 //   * setmaxnreg moves registers from the control warpgroup to the score warpgroups.
 // RoPE angles: pair k's frequency is held as a 64-bit fixed-point fraction of a
 // turn F_k, so position p's phase is (p * F_k mod 2^64) / 2^64 turns: integer
