@@ -488,6 +488,7 @@ __global__ void __launch_bounds__(Lay<I4>::kThreads, 1)
     const int X = wg - 1;
     const int quad = warp & 3;               // TMEM lane quadrant this warp may access
     const int row = quad * 32 + lane;
+    bool slot_lost = false;   // warp-uniform: a score-slot wait gave up
     int pos_next = token_position(a, b, t_begin + row, t_begin + row < t_end);
     float ks_next = 1.f;
     if constexpr (I4)
@@ -506,9 +507,10 @@ __global__ void __launch_bounds__(Lay<I4>::kThreads, 1)
           if (tn < t_end) ks_next = __half2float(a.k_scale[((int64_t)row0 + tn) * a.n_g + g]);
       }
 
-      const bool got = tc::mbar_wait_bounded(&tfull[buf], use & 1, abort_flag, kWaitNs) &&
-                       tc::mbar_wait_bounded(&sfree[buf], (use & 1) ^ 1, abort_flag, kWaitNs);
-      if (tc::named_bar_or(1 + X, kWg, !got)) break;  // one decision for the warpgroup
+      // the score slot is needed only for the final write: wait for the accumulator now and
+      // for the slot after the math, so TMEM goes back to the MMA as early as possible
+      const bool got = tc::mbar_wait_bounded(&tfull[buf], use & 1, abort_flag, kWaitNs);
+      if (tc::named_bar_or(1 + X, kWg, !got || slot_lost)) break;  // one decision for the warpgroup
       tc::tc_fence_after();
 
       // accumulator columns: 2 d + j = dimension d of head j, so (head 0, head 1) of a dimension
@@ -555,10 +557,14 @@ __global__ void __launch_bounds__(Lay<I4>::kThreads, 1)
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&tempty[buf]);
-      sbuf[(buf * 2 + X) * kTile + row] =
-          valid ? make_float2((s0a + s0b) * ks, (s1a + s1b) * ks) : make_float2(-INFINITY, -INFINITY);
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&sready[buf]);
+      // a slot wait that gave up skips the write; the next tile's barrier-OR ends the loop
+      slot_lost = __any_sync(0xffffffffu, !tc::mbar_wait_bounded(&sfree[buf], (use & 1) ^ 1, abort_flag, kWaitNs));
+      if (!slot_lost) {
+        sbuf[(buf * 2 + X) * kTile + row] =
+            valid ? make_float2((s0a + s0b) * ks, (s1a + s1b) * ks) : make_float2(-INFINITY, -INFINITY);
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&sready[buf]);
+      }
     }
   } else if (wg <= 4) {
     // ------------------------------------------------------------ softmax / PV warpgroups
