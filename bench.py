@@ -27,16 +27,16 @@ sys.path.insert(0, ROOT)
 
 METRIC = "decode-attn latency µs & effective KV GB/s at T=4K–64K; % of roofline"
 
-# name -> (config id, T override)
+# name -> (workload in synthetic.gen, T override)
 WORKLOADS = {
-    "config1-tiny-fp32": (1, None),
-    "config2-rope-fp16-b1-t4k": (2, None),
-    "config3-rope-bf16-b8-t16k": (3, 16384),
-    "config3-rope-bf16-b8-t32k": (3, 32768),
-    "config4-absorbed-fp16-b4-t64k": (4, None),
-    "config5-rope-int4-b4-t64k": (5, None),
+    "tiny-fp32-b1-t512": ("TINY_FP32", None),
+    "llama2-7b-rope-fp16-b1-t4k": ("ROPE_FP16", None),
+    "llama2-7b-rope-bf16-b8-t16k": ("ROPE_BF16", 16384),
+    "llama2-7b-rope-bf16-b8-t32k": ("ROPE_BF16", None),
+    "llama2-7b-absorbed-fp16-b4-t64k": ("ABSORBED_FP16", None),
+    "llama2-7b-rope-int4-hadamard-b4-t64k": ("ROPE_INT4", None),
 }
-DEFAULT_WORKLOAD = "config2-rope-fp16-b1-t4k"
+DEFAULT_WORKLOAD = "llama2-7b-rope-fp16-b1-t4k"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -499,8 +499,8 @@ def main(argv=None):
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     from synthetic import gen
-    cid, T = WORKLOADS[args.workload]
-    cfg = gen.CONFIGS[cid] if T is None else gen.CONFIGS[cid].with_(T=T)
+    base, T = WORKLOADS[args.workload]
+    cfg = getattr(gen, base) if T is None else getattr(gen, base).with_(T=T)
     if args.batch is not None:
         cfg = cfg.with_(batch=args.batch)
     if args.tokens is not None:

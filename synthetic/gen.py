@@ -22,9 +22,9 @@ Palu notes evaluate, "实验环境"/"实验结果"):
     because U_r has orthonormal columns, so the latents have the same
     distribution (K and V latents are then drawn independently).
   * q ~ N(0, I) per head; positions 0..T-1.
-Seeds: numpy PCG64 streams spawned from SeedSequence(20261202 + config id), one
-each for W_k, W_v, x, q and W_o; configurations 2-5 are one layer and draw W_k and
-W_v from configuration 2's streams.
+Seeds: numpy PCG64 streams spawned from SeedSequence(20261202 + stream id), one
+each for W_k, W_v, x, q and W_o; the four Llama-2-7B workloads are one layer and
+draw W_k and W_v from the fp16 RoPE workload's streams.
 """
 from __future__ import annotations
 
@@ -42,7 +42,7 @@ EXACT_X_LIMIT = 1 << 26
 
 @dataclasses.dataclass(frozen=True)
 class Config:
-    cid: int
+    stream: int          # seed-stream id (SEED_BASE + stream); the Llama-2-7B layers share weights
     name: str
     batch: int
     n_heads: int
@@ -74,30 +74,28 @@ class Config:
         return dataclasses.replace(self, **kw)
 
 
-CONFIGS = {
-    1: Config(1, "tiny-fp32", 1, 8, 64, 512, 4, 128, 512, "f32", "rope", 64.0),
-    2: Config(2, "llama2-7b-rope-fp16", 1, 32, 128, 4096, 4, 256, 4096, "f16", "rope", 512.0),
-    3: Config(3, "llama2-7b-rope-bf16", 8, 32, 128, 4096, 4, 256, 32768, "bf16", "rope", 512.0),
-    4: Config(4, "llama2-7b-absorbed-fp16", 4, 32, 128, 4096, 4, 256, 65536, "f16", "absorbed", 512.0),
-    5: Config(5, "llama2-7b-rope-int4-hadamard", 4, 32, 128, 4096, 4, 256, 65536, "int4", "rope", 512.0,
-              hadamard=True),
-}
+# The workloads: a tiny fp32 layer (8 heads, d_h 64, hidden 512, rank 128, T 512) and one
+# Llama-2-7B attention layer (32 heads, d_h 128, hidden 4096, group 4, rank 256) in four forms.
+TINY_FP32 = Config(1, "tiny-fp32-b1-t512", 1, 8, 64, 512, 4, 128, 512, "f32", "rope", 64.0)
+ROPE_FP16 = Config(2, "llama2-7b-rope-fp16-b1-t4k", 1, 32, 128, 4096, 4, 256, 4096, "f16", "rope", 512.0)
+ROPE_BF16 = Config(3, "llama2-7b-rope-bf16-b8-t32k", 8, 32, 128, 4096, 4, 256, 32768, "bf16", "rope", 512.0)
+ABSORBED_FP16 = Config(4, "llama2-7b-absorbed-fp16-b4-t64k", 4, 32, 128, 4096, 4, 256, 65536, "f16", "absorbed",
+                       512.0)
+ROPE_INT4 = Config(5, "llama2-7b-rope-int4-hadamard-b4-t64k", 4, 32, 128, 4096, 4, 256, 65536, "int4", "rope",
+                   512.0, hadamard=True)
+ALL = (TINY_FP32, ROPE_FP16, ROPE_BF16, ABSORBED_FP16, ROPE_INT4)
+LLAMA_STREAM = ROPE_FP16.stream
 
 
-def config_by_id(cid: int, **overrides) -> Config:
-    c = CONFIGS[cid]
-    return c.with_(**overrides) if overrides else c
-
-
-def _streams(cid: int):
-    ss = np.random.SeedSequence(SEED_BASE + cid)
+def _streams(stream: int):
+    ss = np.random.SeedSequence(SEED_BASE + stream)
     return [np.random.Generator(np.random.PCG64(s)) for s in ss.spawn(5)]
 
 
-def _weight_seed_id(cid: int) -> int:
-    # Configurations 2-5 describe the same Llama-2-7B layer, so they share its weights;
-    # activations and queries keep per-configuration streams.
-    return 2 if cid in (2, 3, 4, 5) else cid
+def _weight_stream(stream: int) -> int:
+    # the four Llama-2-7B workloads describe the same layer, so they share its weights;
+    # activations and queries keep their own streams
+    return LLAMA_STREAM if stream in (s.stream for s in ALL[1:]) else stream
 
 
 def _haar(rng: np.random.Generator, n: int) -> np.ndarray:
@@ -107,9 +105,9 @@ def _haar(rng: np.random.Generator, n: int) -> np.ndarray:
 
 
 @functools.lru_cache(maxsize=8)
-def _weights(cid: int, hidden: int, tau: float):
+def _weights(stream: int, hidden: int, tau: float):
     """Spectrum-decay W_k, W_v (hidden x hidden), float64."""
-    rk, rv, _, _, _ = _streams(cid)
+    rk, rv, _, _, _ = _streams(stream)
     sig = np.exp(-np.arange(hidden) / tau)
     out = []
     for rng in (rk, rv):
@@ -121,8 +119,8 @@ def _weights(cid: int, hidden: int, tau: float):
 
 @functools.lru_cache(maxsize=8)
 def _factors(cfg_key):
-    cid, hidden, tau, n_g, s, d_h, r, had = cfg_key
-    wk, wv = _weights(cid, hidden, tau)
+    stream, hidden, tau, n_g, s, d_h, r, had = cfg_key
+    wk, wv = _weights(stream, hidden, tau)
     R = scipy.linalg.hadamard(r).astype(np.float64) / math.sqrt(r) if had else None
     res = {}
     for name, w in (("k", wk), ("v", wv)):
@@ -145,11 +143,11 @@ def _factors(cfg_key):
 
 def weights(cfg: Config):
     """(W_k, W_v) float64 full projection matrices of the configuration."""
-    return _weights(_weight_seed_id(cfg.cid), cfg.hidden, cfg.sigma_tau)
+    return _weights(_weight_stream(cfg.stream), cfg.hidden, cfg.sigma_tau)
 
 
 def factors(cfg: Config):
-    key = (_weight_seed_id(cfg.cid), cfg.hidden, cfg.sigma_tau, cfg.n_groups, cfg.group_size, cfg.head_dim,
+    key = (_weight_stream(cfg.stream), cfg.hidden, cfg.sigma_tau, cfg.n_groups, cfg.group_size, cfg.head_dim,
            cfg.rank, cfg.hadamard)
     return _factors(key)
 
@@ -168,7 +166,7 @@ def make_inputs(cfg: Config, *, exact_x: bool | None = None, q_scale: float = 1.
     B, T, d = cfg.batch, cfg.T, cfg.hidden
     n_g, r, s, d_h = cfg.n_groups, cfg.rank, cfg.group_size, cfg.head_dim
     fac, R = factors(cfg)
-    _, _, rx, rq, ro = _streams(cfg.cid)
+    _, _, rx, rq, ro = _streams(cfg.stream)
     if exact_x is None:
         exact_x = B * T * d <= EXACT_X_LIMIT
     out = {"cfg": cfg}

@@ -30,7 +30,7 @@ def _rank_main(rank, world, port, out):
         # the reference arm: rank 0 runs the oracle sample, the others return without work
         args = type("A", (), {"steps": 1, "warmup": 1})()
         from synthetic import gen
-        res = bench.run_reference(args, gen.CONFIGS[1], "config1-tiny-fp32")
+        res = bench.run_reference(args, gen.TINY_FP32, "tiny-fp32-b1-t512")
         out[world + rank] = None if res is None else res["impl"]
     finally:
         dist.destroy_process_group()

@@ -14,8 +14,8 @@ def _gpu(cuda_device):
     return cuda_device
 
 
-def test_config1_tiny_fp32_full():
-    c = Case(gen.CONFIGS[1])
+def test_tiny_fp32_full():
+    c = Case(gen.TINY_FP32)
     out, lse = c.run_gpu()
     ref, lse_ref = c.run_oracle()
     assert_close(out, ref, lse, lse_ref, f32=True)
@@ -23,7 +23,7 @@ def test_config1_tiny_fp32_full():
 
 @pytest.mark.parametrize("T", [1, 2, 127, 128, 129, 1000])
 def test_rope_fp16_tile_edges(T):
-    cfg = gen.CONFIGS[2].with_(T=T, batch=2)
+    cfg = gen.ROPE_FP16.with_(T=T, batch=2)
     c = Case(cfg, seq_lens=[T, max(1, (T * 2) // 3)])
     out, lse = c.run_gpu()
     ref, lse_ref = c.run_oracle()
@@ -31,7 +31,7 @@ def test_rope_fp16_tile_edges(T):
 
 
 def test_rope_bf16_explicit_positions_query_position_and_empty_row():
-    cfg = gen.CONFIGS[3].with_(T=300, batch=3)
+    cfg = gen.ROPE_BF16.with_(T=300, batch=3)
     rng = np.random.default_rng(5)
     pos = np.stack([rng.permutation(5000)[:300] for _ in range(3)]).astype(np.int32)
     c = Case(cfg, seq_lens=[300, 17, 0], positions=pos, q_pos=[4999, 123, 0], max_position=5000)
@@ -42,7 +42,7 @@ def test_rope_bf16_explicit_positions_query_position_and_empty_row():
 
 
 def test_rope_default_query_position_with_positions():
-    cfg = gen.CONFIGS[2].with_(T=200, batch=2)
+    cfg = gen.ROPE_FP16.with_(T=200, batch=2)
     pos = (np.arange(200)[None, :] * 3 + np.array([[7], [1000]])).astype(np.int32)
     c = Case(cfg, seq_lens=[200, 150], positions=pos, max_position=2000)
     out, lse = c.run_gpu()
@@ -51,7 +51,7 @@ def test_rope_default_query_position_with_positions():
 
 
 def test_absorbed_fp16_ragged():
-    cfg = gen.CONFIGS[4].with_(T=1000, batch=2)
+    cfg = gen.ABSORBED_FP16.with_(T=1000, batch=2)
     c = Case(cfg, seq_lens=[1000, 333])
     out, lse = c.run_gpu()
     ref, lse_ref = c.run_oracle()
@@ -59,7 +59,7 @@ def test_absorbed_fp16_ragged():
 
 
 def test_absorbed_bf16_ragged():
-    cfg = gen.CONFIGS[4].with_(T=1000, batch=3, latent_dtype="bf16")
+    cfg = gen.ABSORBED_FP16.with_(T=1000, batch=3, latent_dtype="bf16")
     c = Case(cfg, seq_lens=[1000, 1, 517])
     out, lse = c.run_gpu()
     ref, lse_ref = c.run_oracle()
@@ -67,16 +67,16 @@ def test_absorbed_bf16_ragged():
 
 
 def test_absorbed_int4_on_cuda_cores():
-    cfg = gen.CONFIGS[4].with_(T=300, batch=2, latent_dtype="int4")
+    cfg = gen.ABSORBED_FP16.with_(T=300, batch=2, latent_dtype="int4")
     c = Case(cfg, seq_lens=[300, 77])
     out, lse = c.run_gpu()
     ref, lse_ref = c.run_oracle()
     assert_close(out, ref, lse, lse_ref)
 
 
-@pytest.mark.parametrize("cid", [2, 4])
-def test_float32_query(cid):
-    cfg = gen.CONFIGS[cid].with_(T=500, batch=2)
+@pytest.mark.parametrize("base", [gen.ROPE_FP16, gen.ABSORBED_FP16], ids=lambda c: c.name)
+def test_float32_query(base):
+    cfg = base.with_(T=500, batch=2)
     c = Case(cfg, seq_lens=[500, 250], q_dtype="f32")
     out, lse = c.run_gpu()
     ref, lse_ref = c.run_oracle()
@@ -84,7 +84,7 @@ def test_float32_query(cid):
 
 
 def test_peaked_softmax_stress():
-    cfg = gen.CONFIGS[2].with_(T=512, batch=1)
+    cfg = gen.ROPE_FP16.with_(T=512, batch=1)
     c = Case(cfg, q_scale=8.0)
     out, lse = c.run_gpu()
     ref, lse_ref = c.run_oracle()
@@ -92,7 +92,7 @@ def test_peaked_softmax_stress():
 
 
 def test_split_plan_does_not_change_result():
-    cfg = gen.CONFIGS[2].with_(T=700, batch=1)
+    cfg = gen.ROPE_FP16.with_(T=700, batch=1)
     c = Case(cfg, capacity=4096)
     a, _ = c.run_gpu()
     b, _ = c.run_gpu(max_seq_len=4096)
@@ -104,7 +104,7 @@ def test_split_plan_does_not_change_result():
 def test_float_append_matches_round_to_nearest():
     import torch
     for lat in ("f16", "bf16"):
-        cfg = gen.CONFIGS[2].with_(T=64, batch=2, latent_dtype=lat)
+        cfg = gen.ROPE_FP16.with_(T=64, batch=2, latent_dtype=lat)
         c = Case(cfg)
         want = gen.storage_round(c.inp["hk"], lat)
         got = c.cache.hk[:, :64].cpu()
@@ -113,7 +113,7 @@ def test_float_append_matches_round_to_nearest():
 
 def test_int4_append_bit_exact_and_dequant():
     import torch
-    cfg = gen.CONFIGS[5].with_(T=300, batch=2)
+    cfg = gen.ROPE_INT4.with_(T=300, batch=2)
     c = Case(cfg)
     pk, sk, pv, sv = c.ref_packed
     np.testing.assert_array_equal(c.cache.hk[:, :300].cpu().numpy(), pk)
@@ -130,7 +130,7 @@ def test_int4_append_bit_exact_and_dequant():
 
 
 def test_int4_rope_hadamard_ragged():
-    cfg = gen.CONFIGS[5].with_(T=700, batch=2)
+    cfg = gen.ROPE_INT4.with_(T=700, batch=2)
     c = Case(cfg, seq_lens=[700, 259])
     out, lse = c.run_gpu()
     ref, lse_ref = c.run_oracle()
@@ -140,7 +140,7 @@ def test_int4_rope_hadamard_ragged():
 @pytest.mark.parametrize("T", [64, 127, 128, 129, 1000])
 def test_int4_rope_tile_edges(T):
     # batch * capacity >= 128: the tensor-core kernel with the int4 converter
-    cfg = gen.CONFIGS[5].with_(T=T, batch=2)
+    cfg = gen.ROPE_INT4.with_(T=T, batch=2)
     c = Case(cfg, seq_lens=[T, max(1, (T * 2) // 3)])
     out, lse = c.run_gpu()
     ref, lse_ref = c.run_oracle()
@@ -150,7 +150,7 @@ def test_int4_rope_tile_edges(T):
 def test_int4_peaked_softmax_stress():
     # a few tokens dominate: the int4 p H_v path quantises each warp's 16 weights to 15 bits
     # against their largest, so the error stays a small fraction of the dominant term
-    cfg = gen.CONFIGS[5].with_(T=900, batch=2)
+    cfg = gen.ROPE_INT4.with_(T=900, batch=2)
     c = Case(cfg, seq_lens=[900, 611], q_scale=8.0)
     out, lse = c.run_gpu()
     ref, lse_ref = c.run_oracle()
@@ -158,7 +158,7 @@ def test_int4_peaked_softmax_stress():
 
 
 def test_int4_rope_positions_and_split_plan():
-    cfg = gen.CONFIGS[5].with_(T=700, batch=2)
+    cfg = gen.ROPE_INT4.with_(T=700, batch=2)
     rng = np.random.default_rng(11)
     pos = np.stack([rng.permutation(3000)[:700] for _ in range(2)]).astype(np.int32)
     c = Case(cfg, seq_lens=[700, 450], positions=pos, q_pos=[2999, 5], capacity=4096, max_position=3000)
@@ -171,7 +171,7 @@ def test_int4_rope_positions_and_split_plan():
 
 def test_device_error_word_on_bad_position():
     from rank_kv_cache_gb300 import palu as P
-    cfg = gen.CONFIGS[2].with_(T=64, batch=1)
+    cfg = gen.ROPE_FP16.with_(T=64, batch=1)
     pos = np.arange(64, dtype=np.int32)[None, :].copy()
     pos[0, 10] = 100000  # outside the 64-entry table
     c = Case(cfg, positions=pos)
@@ -191,16 +191,18 @@ def _sample_heads(B, n, k=6, seed=0):
     return sorted(hs)
 
 
-def test_full_config2_all_heads():
-    c = Case(gen.CONFIGS[2])
+def test_full_rope_fp16_b1_t4k_all_heads():
+    c = Case(gen.ROPE_FP16)
     out, lse = c.run_gpu()
     ref, lse_ref = c.run_oracle()
     assert_close(out, ref, lse, lse_ref)
 
 
-@pytest.mark.parametrize("cid,T", [(3, 16384), (3, 32768), (4, 65536), (5, 65536)])
-def test_full_size_sampled_heads(cid, T):
-    cfg = gen.CONFIGS[cid].with_(T=T)
+@pytest.mark.parametrize("base,T", [(gen.ROPE_BF16, 16384), (gen.ROPE_BF16, 32768), (gen.ABSORBED_FP16, 65536),
+                                    (gen.ROPE_INT4, 65536)], ids=["rope-bf16-b8-t16k", "rope-bf16-b8-t32k",
+                                                                  "absorbed-fp16-b4-t64k", "rope-int4-b4-t64k"])
+def test_full_size_sampled_heads(base, T):
+    cfg = base.with_(T=T)
     c = Case(cfg)
     out, lse = c.run_gpu()
     heads = _sample_heads(cfg.batch, cfg.n_heads)
@@ -208,13 +210,13 @@ def test_full_size_sampled_heads(cid, T):
     assert_close(out, ref, lse, lse_ref, heads=heads)
 
 
-@pytest.mark.parametrize("cid,kernel", [(1, "SIMT"), (2, "TC_ROPE"), (3, "TC_ROPE"), (4, "TMA_ABSORBED"),
-                                        (5, "TC_ROPE")])
-def test_kernel_choice_per_workload(cid, kernel):
+@pytest.mark.parametrize("cfg,kernel", [(gen.TINY_FP32, "SIMT"), (gen.ROPE_FP16, "TC_ROPE"), (gen.ROPE_BF16, "TC_ROPE"),
+                                        (gen.ABSORBED_FP16, "TMA_ABSORBED"), (gen.ROPE_INT4, "TC_ROPE")],
+                         ids=lambda x: x.name if hasattr(x, "name") else x)
+def test_kernel_choice_per_workload(cfg, kernel):
     # the fast kernels must be the ones the full-size workloads run on
     import torch
     from rank_kv_cache_gb300 import palu as P
-    cfg = gen.CONFIGS[cid]
     bk = torch.zeros((cfg.n_groups, cfg.rank, cfg.group_size * cfg.head_dim),
                      dtype={"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[cfg.bk_dtype],
                      device="cuda")
@@ -232,7 +234,7 @@ def test_bounded_wait_gives_up_and_reports_timeout():
     # CTAs unwind, and the error word reports PALU_ERR_TIMEOUT; the context stays usable
     import torch
     from rank_kv_cache_gb300 import palu as P
-    cfg = gen.CONFIGS[2].with_(T=300, batch=2)
+    cfg = gen.ROPE_FP16.with_(T=300, batch=2)
     c = Case(cfg)
     stall = P.PaluAttention(c.bk_t.to(c.dev), n_heads=cfg.n_heads, head_dim=cfg.head_dim,
                             group_size=cfg.group_size, rank_k=cfg.rank, rank_v=cfg.rank, latent_dtype="f16",
@@ -256,7 +258,7 @@ def test_cache_saved_and_reloaded_decodes_identically():
     # into fresh device buffers gives the same bits
     import torch
     from rank_kv_cache_gb300 import palu as P
-    cfg = gen.CONFIGS[5].with_(T=400, batch=2)
+    cfg = gen.ROPE_INT4.with_(T=400, batch=2)
     c = Case(cfg, seq_lens=[400, 123])
     out1, lse1 = c.run_gpu()
     saved = {k: getattr(c.cache, k).cpu() for k in ("hk", "hv", "k_scale", "v_scale")}

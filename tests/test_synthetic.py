@@ -9,17 +9,16 @@ from synthetic import gen
 
 
 def test_configs_follow_llama2_7b_group_shapes():
-    for cid in (2, 3, 4, 5):
-        c = gen.CONFIGS[cid]
+    for c in (gen.ROPE_FP16, gen.ROPE_BF16, gen.ABSORBED_FP16, gen.ROPE_INT4):
         assert (c.n_heads, c.head_dim, c.hidden, c.group_size, c.rank) == (32, 128, 4096, 4, 256)
         # G-LRD concatenation of s = 4 heads: a 4096 x 512 matrix (Palu notes, "补充细节")
         assert (c.hidden, c.head_dim * c.group_size) == (4096, 512)
-    c1 = gen.CONFIGS[1]
+    c1 = gen.TINY_FP32
     assert (c1.n_heads, c1.head_dim, c1.hidden, c1.n_groups, c1.rank, c1.T) == (8, 64, 512, 2, 128, 512)
 
 
 def test_tiny_workload_deterministic_and_consistent():
-    cfg = gen.CONFIGS[1]
+    cfg = gen.TINY_FP32
     a = gen.make_inputs(cfg, with_x=True)
     b = gen.make_inputs(cfg, with_x=True)
     np.testing.assert_array_equal(a["hk"], b["hk"])
@@ -40,9 +39,9 @@ def test_tiny_workload_deterministic_and_consistent():
 
 
 def test_hadamard_fold_in_generator_preserves_weights():
-    cfg = gen.CONFIGS[1].with_(hadamard=True)
+    cfg = gen.TINY_FP32.with_(hadamard=True)
     a = gen.make_inputs(cfg)
-    plain = gen.make_inputs(gen.CONFIGS[1])
+    plain = gen.make_inputs(gen.TINY_FP32)
     for g in range(cfg.n_groups):
         np.testing.assert_allclose(a["ak"][g] @ a["bk"][g], plain["ak"][g] @ plain["bk"][g], atol=1e-12)
     R = O.hadamard(cfg.rank)
@@ -51,7 +50,7 @@ def test_hadamard_fold_in_generator_preserves_weights():
 
 def test_equivalent_latent_draw_matches_covariance():
     # The large-workload draw must have the covariance of x A: A^T A = diag(S_r).
-    cfg = gen.CONFIGS[1].with_(T=20000)
+    cfg = gen.TINY_FP32.with_(T=20000)
     a = gen.make_inputs(cfg, exact_x=False)
     h = a["hk"][0, :, 0, :].astype(np.float64)
     cov = h.T @ h / h.shape[0]
