@@ -28,7 +28,8 @@ struct DecodeArgs {
   // workspace-resident operands
   const float* qbuf;          // [B][n][dh] rotated (rope) or [B][n][rk] absorbed; pre-scaled by log2(e)/sqrt(dh)
   const void* bk;             // [n_g][rk][s*dh], bk_dtype
-  const void* bkt;            // [n_g][s*dh][rk], MMA dtype (K-major operand for tcgen05)
+  const void* bkt;            // [n_g][s*dh][rk], MMA dtype: the K-major tcgen05 operand, rows of each head
+                              // pair interleaved by head, ranks permuted in eights for int4 caches
   const float2* rope;         // [max_pos][dh/2] (cos, sin)
   const uint64_t* phase;      // [dh/2] frequency of each pair as a 64-bit fraction of a turn
   // query (read directly by kernels that rotate it themselves)
