@@ -4,8 +4,11 @@
 One step = one decode step of one attention layer over a latent KV cache already
 resident in HBM: append the new token's K/V latents (quantising them for int4
 caches), prepare the query, run the decode-attention kernel over all cached
-tokens, and merge the split-T partials. The default workload is the Llama-2-7B
-RoPE layer with fp16 latents at batch 1 and T = 4096 tokens.
+tokens, and merge the split-T partials. The headline workload is the Llama-2-7B
+RoPE layer with int4 latents (Hadamard-folded factors) at batch 4 and T = 65536;
+``per_config`` in the same line times every other workload of the benchmark
+(T = 512 to 64K) the same way, each with its own roofline fraction and oracle
+baseline.
 
 Prints ONE JSON line (rank 0). ``--impl reference`` times the float64 CPU oracle
 instead, on a bounded sample of the same workload.
@@ -20,6 +23,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -36,8 +40,23 @@ WORKLOADS = {
     "llama2-7b-absorbed-fp16-b4-t64k": ("ABSORBED_FP16", None),
     "llama2-7b-rope-int4-hadamard-b4-t64k": ("ROPE_INT4", None),
 }
-DEFAULT_WORKLOAD = "llama2-7b-rope-fp16-b1-t4k"
+DEFAULT_WORKLOAD = "llama2-7b-rope-int4-hadamard-b4-t64k"
+PER_CONFIG_ORDER = ("tiny-fp32-b1-t512", "llama2-7b-rope-fp16-b1-t4k", "llama2-7b-rope-bf16-b8-t16k",
+                    "llama2-7b-rope-bf16-b8-t32k", "llama2-7b-absorbed-fp16-b4-t64k",
+                    "llama2-7b-rope-int4-hadamard-b4-t64k")
+SINGLE_CORE_ORACLE = ("tiny-fp32-b1-t512", "llama2-7b-rope-fp16-b1-t4k")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def config_of(name, batch=None, tokens=None):
+    from synthetic import gen
+    base, T = WORKLOADS[name]
+    cfg = getattr(gen, base) if T is None else getattr(gen, base).with_(T=T)
+    if batch is not None:
+        cfg = cfg.with_(batch=batch)
+    if tokens is not None:
+        cfg = cfg.with_(T=tokens)
+    return cfg
 
 
 # ---------------------------------------------------------------------------
@@ -85,19 +104,38 @@ def load_peaks():
 
 
 def roofline_for(cfg, work, kernel_ms, peaks, peaks_src, long_step):
+    """The slower of latent bytes over HBM and (RoPE) rebuild flops over the tensor peak bounds
+    the decode kernel; achieved = that resource's algorithmic work / the kernel's duration."""
     hbm = float(peaks["hbm_gbs"])
-    tc = float(peaks["bf16_tflops_sustained" if long_step else "bf16_tflops"])  # fp16 = bf16 nominal rate
+    tc_key = "bf16_tflops_sustained" if long_step else "bf16_tflops"
+    tc = float(peaks[tc_key])  # fp16 = bf16 nominal rate
     t_hbm = work["decode_bytes"] / (hbm * 1e9)
     t_tc = work["flops"] / (tc * 1e12) if cfg.mode == "rope" else 0.0
     sec = kernel_ms / 1e3
     if t_tc > t_hbm:
         ach = work["flops"] / sec / 1e12
         return {"bound": "tensor", "achieved": round(ach, 2), "peak": tc, "unit": "TFLOP/s",
-                "frac": round(ach / tc, 4), "traffic": None,
-                "peak_source": f"{'bf16_tflops_sustained' if long_step else 'bf16_tflops'} of {peaks_src}"}
+                "frac": round(ach / tc, 4), "traffic": None, "roofline_us": round(t_tc * 1e6, 2),
+                "peak_source": f"{tc_key} of {peaks_src}"}
     ach = work["decode_bytes"] / sec / 1e9
     return {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s", "frac": round(ach / hbm, 4),
-            "traffic": None, "peak_source": f"hbm_gbs of {peaks_src}"}
+            "traffic": None, "roofline_us": round(t_hbm * 1e6, 2), "peak_source": f"hbm_gbs of {peaks_src}"}
+
+
+def pct(xs, q):
+    """q-th percentile (0..100) of a non-empty list, linear interpolation."""
+    s = sorted(xs)
+    if len(s) == 1:
+        return s[0]
+    k = (len(s) - 1) * q / 100.0
+    lo, hi = int(math.floor(k)), int(math.ceil(k))
+    return s[lo] + (s[hi] - s[lo]) * (k - lo)
+
+
+def stats_us(ms_list):
+    us = [m * 1e3 for m in ms_list]
+    return {"median": round(pct(us, 50), 2), "p10": round(pct(us, 10), 2), "p90": round(pct(us, 90), 2),
+            "mean": round(statistics.mean(us), 2), "n": len(us)}
 
 
 # ---------------------------------------------------------------------------
@@ -233,33 +271,56 @@ def job_throughput_gbs(world, bytes_per_rank_step, ms_per_step):
 
 
 class GpuWorkload:
-    """Device-resident workload: cache filled through the append kernel, per-step inputs."""
+    """Device-resident workload: the latent cache drawn on the device and filled through the
+    append kernel one batch row at a time, plus the per-step inputs."""
 
     def __init__(self, cfg, device):
         import torch
         from rank_kv_cache_gb300 import palu as P
         from synthetic import gen
-        self.cfg, self.dev = cfg, device
-        inp = gen.make_inputs(cfg)
-        B, T = cfg.batch, cfg.T
+        self.cfg, self.dev, self.P = cfg, device, P
+        B, T, n_g, r = cfg.batch, cfg.T, cfg.n_groups, cfg.rank
         lat = cfg.latent_dtype
-        self.attn = P.PaluAttention(gen.storage_round(inp["bk"], cfg.bk_dtype).to(device), n_heads=cfg.n_heads,
-                                    head_dim=cfg.head_dim, group_size=cfg.group_size, rank_k=cfg.rank,
-                                    rank_v=cfg.rank, latent_dtype=lat, q_dtype=cfg.q_dtype, mode=cfg.mode,
-                                    rope_theta=cfg.theta, max_batch=B, max_tokens=T)
-        self.cache = P.LatentCache(B, T, cfg.n_groups, cfg.rank, cfg.rank, lat, device=device)
-        src_dt = "f32" if lat == "int4" else lat
-        hk = gen.storage_round(inp["hk"], src_dt).to(device)
-        hv = gen.storage_round(inp["hv"], src_dt).to(device)
-        zero = torch.zeros(B, dtype=torch.int32, device=device)
-        self.attn.append(self.cache, hk, hv, zero)            # prefill the cache (not timed)
-        self.hk_new = hk[:, T - 1:T].contiguous()             # the step's new token (rewritten at slot T-1)
-        self.hv_new = hv[:, T - 1:T].contiguous()
-        del hk, hv
+        fac, _ = gen.factors(cfg)
+        self.bk_host = gen.storage_round(fac["k"][1], cfg.bk_dtype)
+        self.attn = P.PaluAttention(self.bk_host.to(device), n_heads=cfg.n_heads, head_dim=cfg.head_dim,
+                                    group_size=cfg.group_size, rank_k=r, rank_v=r, latent_dtype=lat,
+                                    q_dtype=cfg.q_dtype, mode=cfg.mode, rope_theta=cfg.theta, max_batch=B,
+                                    max_tokens=T)
+        self.cache = P.LatentCache(B, T, n_g, r, r, lat, device=device)
+        src_dt = "f32" if lat in ("int4", "f32") else lat
+        tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[src_dt]
+        zero = torch.zeros(1, dtype=torch.int32, device=device)
+        new_k, new_v = [], []
+        self.sample_hk = self.sample_hv = None
+        row_bytes_k = self.cache.hk[0].numel() * self.cache.hk.element_size()
+        row_bytes_v = self.cache.hv[0].numel() * self.cache.hv.element_size()
+        for b, (zk, zv) in enumerate(zip(gen.latent_rows_torch(cfg, device, "k"),
+                                         gen.latent_rows_torch(cfg, device, "v"))):
+            if b == 0:   # the oracle's sample: group 0 of batch row 0, unrounded float32
+                self.sample_hk = zk[:, 0, :].cpu().numpy()
+                self.sample_hv = zv[:, 0, :].cpu().numpy()
+            hk, hv = zk.to(tdt)[None], zv.to(tdt)[None]
+            new_k.append(hk[:, T - 1:T].clone())
+            new_v.append(hv[:, T - 1:T].clone())
+            c = self.cache.c_struct()
+            c.hk += b * row_bytes_k
+            c.hv += b * row_bytes_v
+            if lat == "int4":
+                c.k_scale += b * T * n_g * 2
+                c.v_scale += b * T * n_g * 2
+            P.check(P.palu_append_latents(self.attn.handle, c, hk.data_ptr(), hv.data_ptr(), P.DTYPES[src_dt],
+                                          zero.data_ptr(), 1, T, int(torch.cuda.current_stream().cuda_stream)),
+                    "prefill append")
+            del zk, zv, hk, hv
+        torch.cuda.synchronize()
+        self.hk_new = torch.cat(new_k).contiguous()       # the step's new token (rewritten at slot T-1)
+        self.hv_new = torch.cat(new_v).contiguous()
         self.slot = torch.full((B,), T - 1, dtype=torch.int32, device=device)
         self.seq = torch.full((B,), T, dtype=torch.int32, device=device)
-        self.q = gen.storage_round(inp["q"], cfg.q_dtype).to(device)
-        self.out = torch.empty((B, cfg.n_heads, cfg.rank), dtype=torch.float32, device=device)
+        self.q_host = gen.draw_query(cfg)
+        self.q = gen.storage_round(self.q_host, cfg.q_dtype).to(device)
+        self.out = torch.empty((B, cfg.n_heads, r), dtype=torch.float32, device=device)
         self.lse = torch.empty((B, cfg.n_heads), dtype=torch.float32, device=device)
         torch.cuda.synchronize()
 
@@ -267,20 +328,48 @@ class GpuWorkload:
         self.attn.append(self.cache, self.hk_new, self.hv_new, self.slot)
         self.attn.decode(self.q, self.cache, self.seq, max_seq_len=self.cfg.T, out=self.out, lse=self.lse)
 
+    def plan(self):
+        return self.attn.plan(self.cfg.T, self.cfg.batch, self.cfg.T)
+
     @property
     def launches_per_step(self):
         # one append launch (K and V together) + the decode call's own launches: the split
         # merge runs inside the decode kernel; the absorbed and CUDA-core kernels add a
         # query-preparation launch
-        kernel, _, launches = self.attn.plan(self.cfg.T, self.cfg.batch, self.cfg.T)
-        return 1 + launches
+        return 1 + self.plan()[2]
 
     @property
     def kernel_name(self):
-        from rank_kv_cache_gb300 import palu as P
-        kernel = self.attn.plan(self.cfg.T, self.cfg.batch, self.cfg.T)[0]
+        P = self.P
         return {P.PALU_KERNEL_TC_ROPE: "decode_tc_kernel", P.PALU_KERNEL_TMA_ABSORBED: "decode_abs_kernel",
-                P.PALU_KERNEL_SIMT: "decode_simt_kernel"}[kernel]
+                P.PALU_KERNEL_SIMT: "decode_simt_kernel"}[self.plan()[0]]
+
+    def oracle_sample(self):
+        return OracleSample(self.cfg, self.sample_hk, self.sample_hv, self.q_host, self.bk_host)
+
+    def close(self):
+        self.attn.close()
+
+
+def timed_steps(wl, n, flush, clock_gpu=None):
+    """n device-timed steps, L2 flushed before each: (step ms list, decode-kernel ms list, clocks)."""
+    import torch
+    P = wl.P
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    P.check(P.palu_attn_trace_enable(wl.attn.handle, 1))
+    torch.cuda.synchronize()
+    with ClockSampler(clock_gpu if clock_gpu is not None else 0) as clk:
+        for i in range(n):
+            flush.zero_()
+            ev[i][0].record()
+            wl.step()
+            ev[i][1].record()
+        torch.cuda.synchronize()
+    st, kms = P.palu_attn_trace_times(wl.attn.handle)
+    P.check(st, "palu_attn_trace_times")
+    P.check(P.palu_attn_trace_enable(wl.attn.handle, 0))
+    wl.attn.check_device()
+    return [a.elapsed_time(b) for a, b in ev], kms, clk.summary()
 
 
 def run_gpu(args, cfg, name):
@@ -321,13 +410,13 @@ def run_gpu(args, cfg, name):
         wall = time.perf_counter() - t0
     if dist:
         dist.barrier()
-    st, n_tr, tr_ms = P.palu_attn_trace_read(wl.attn.handle)
+    st, kernel_ms_list = P.palu_attn_trace_times(wl.attn.handle)
     P.check(st)
     P.palu_attn_trace_enable(wl.attn.handle, 0)
     step_ms = [a.elapsed_time(b) for a, b in ev]
     tot_ms = max_over_ranks(sum(step_ms), dist, dev)
     ms_per_step = tot_ms / K
-    kernel_ms = tr_ms / max(n_tr, 1)
+    kernel_ms = statistics.mean(kernel_ms_list) if kernel_ms_list else float("nan")
     wl.attn.check_device()
 
     # end-to-end through the public API: pinned host inputs in, result back to host, every step
@@ -358,6 +447,8 @@ def run_gpu(args, cfg, name):
     roof = roofline_for(cfg, work, kernel_ms, peaks, peaks_src, long_step=ms_per_step > 10.0)
     roof["kernel"] = wl.kernel_name
     roof["traffic"] = recorded_traffic(name, wl.kernel_name, cfg)
+    roof["duration"] = "mean decode-kernel launch over the timed steps (CUDA events on the launch stream)"
+    kernel, n_splits, launches = wl.plan()
     result = {
         "metric": METRIC,
         "value": round(job_throughput_gbs(world, work["decode_bytes"], ms_per_step), 2),
@@ -371,18 +462,19 @@ def run_gpu(args, cfg, name):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": cfg.latent_dtype,
-        "data": "synthetic (seeded spectrum-decay weights, Gaussian activations and queries)",
+        "data": "synthetic (seeded spectrum-decay weights, Gaussian latents drawn on the device, Gaussian queries)",
         "config": {"workload": name, "batch": cfg.batch, "tokens": cfg.T, "heads": cfg.n_heads,
                    "head_dim": cfg.head_dim, "group_size": cfg.group_size, "rank": cfg.rank,
                    "latent_dtype": cfg.latent_dtype, "mode": cfg.mode, "hadamard": cfg.hadamard,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed (512 MB write) before every timed step",
                    "bytes_per_step": work["decode_bytes"], "flops_per_step": work["flops"],
-                   "dense_fp16_kv_bytes_per_step": work["dense_fp16_kv_bytes"]},
+                   "dense_fp16_kv_bytes_per_step": work["dense_fp16_kv_bytes"], "n_splits": n_splits},
         "dense_equiv_gbs": round(job_throughput_gbs(world, work["dense_fp16_kv_bytes"], ms_per_step), 1),
         "roofline": roof,
-        "kernel_us": round(kernel_ms * 1e3, 2),
-        "kernel_launches_traced": n_tr,
+        "kernel_us": stats_us(kernel_ms_list),
+        "step_us": stats_us(step_ms),
+        "kernel_launches_traced": len(kernel_ms_list),
         "e2e": {"value": round(job_throughput_gbs(world, work["decode_bytes"], e2e_step), 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_step, 6),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke},
@@ -391,11 +483,78 @@ def run_gpu(args, cfg, name):
         "wall_s_timed_region": round(wall, 4),
     }
     if rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(cfg, work, budget_s=args.cpu_seconds)
+        sample = wl.oracle_sample()
+        result["cpu_baseline"] = cpu_baseline(sample, work, budget_s=args.cpu_seconds)
+        result["parity_sample"] = sample.compare(wl.out.cpu().double().numpy())
+    headline_entry = per_config_entry(name, cfg, work, step_ms, kernel_ms_list, clk.summary(), wl, peaks, peaks_src,
+                                      result.get("cpu_baseline"), result.get("parity_sample"))
+    wl.close()
+    del wl
+    torch.cuda.empty_cache()
+    if rank == 0 and world == 1 and not args.no_per_config:
+        result["per_config"] = run_per_config(args, dev, flush, name, headline_entry, peaks, peaks_src)
     if dist:
         dist.barrier()
         dist.destroy_process_group()
     return result if rank == 0 else None
+
+
+def per_config_entry(name, cfg, work, step_ms, kernel_ms, clocks, wl, peaks, peaks_src, cpu=None, parity=None):
+    med = pct(kernel_ms, 50)
+    roof = roofline_for(cfg, work, med, peaks, peaks_src, long_step=False)
+    roof["traffic"] = recorded_traffic(name, wl.kernel_name, cfg)
+    roof["duration"] = "median decode-kernel launch"
+    kernel, n_splits, launches = wl.plan()
+    e = {"batch": cfg.batch, "tokens": cfg.T, "latent_dtype": cfg.latent_dtype, "mode": cfg.mode,
+         "kernel": wl.kernel_name, "n_splits": n_splits, "gpu_launches_per_step": 1 + launches,
+         "decode_kernel_us": stats_us(kernel_ms), "step_us": stats_us(step_ms),
+         "latent_gbs": round(work["decode_bytes"] / (med / 1e3) / 1e9, 1),
+         "dense_equiv_gbs": round(work["dense_fp16_kv_bytes"] / (med / 1e3) / 1e9, 1),
+         "bytes": work["decode_bytes"], "flops": work["flops"], "roofline": roof, "clocks": clocks}
+    if cpu is not None:
+        e["cpu_baseline"] = cpu
+    if parity is not None:
+        e["parity_sample"] = parity
+    return e
+
+
+def run_per_config(args, dev, flush, headline, headline_entry, peaks, peaks_src):
+    """Every benchmark workload at its full size, one after the other: 10 warm-up steps, then at
+    least 50 timed steps (500 at T <= 4K), L2 flushed before each; median/p10/p90 of the decode
+    kernel and of the step, roofline, recorded traffic, clocks and the oracle's CPU baseline."""
+    import torch
+    out = {}
+    for name in PER_CONFIG_ORDER:
+        if name == headline:
+            out[name] = headline_entry
+            continue
+        cfg = config_of(name)
+        t_gen = time.perf_counter()
+        wl = GpuWorkload(cfg, dev)
+        gen_s = time.perf_counter() - t_gen
+        for _ in range(10):
+            flush.zero_()
+            wl.step()
+        torch.cuda.synchronize()
+        n = 500 if cfg.T <= 4096 else max(50, args.per_config_steps)
+        step_ms, kms, clocks = timed_steps(wl, n, flush, dev.index)
+        work = step_work(cfg)
+        cpu = parity = None
+        if not args.no_cpu_baseline:
+            sample = wl.oracle_sample()
+            cpu = cpu_baseline(sample, work, budget_s=args.per_config_cpu_seconds)
+            parity = sample.compare(wl.out.cpu().double().numpy())
+            if name in SINGLE_CORE_ORACLE:
+                cpu["single_core"] = single_core_oracle(sample, work, args.per_config_cpu_seconds)
+        e = per_config_entry(name, cfg, work, step_ms, kms, clocks, wl, peaks, peaks_src, cpu, parity)
+        e["setup_s"] = round(gen_s, 2)
+        out[name] = e
+        print(f"[bench] {name}: decode kernel median {e['decode_kernel_us']['median']} us, "
+              f"{e['roofline']['bound']} frac {e['roofline']['frac']}", file=sys.stderr, flush=True)
+        wl.close()
+        del wl
+        torch.cuda.empty_cache()
+    return out
 
 
 # ---------------------------------------------------------------------------
@@ -414,67 +573,123 @@ def _blas_threads():
 
 
 class OracleSample:
-    """The oracle on storage-rounded inputs of the workload, one (batch, head) at a time."""
+    """The oracle on one G-LRD group (batch row 0, group 0) of the workload: the s heads that read
+    it, over all T tokens, on storage-rounded inputs (int4: the oracle's own quantisation)."""
 
-    def __init__(self, cfg):
+    def __init__(self, cfg, hk, hv, q, bk):
         import numpy as np
         from oracle import palu_oracle as O
         from synthetic import gen
         self.O, self.np, self.cfg = O, np, cfg
-        inp = gen.make_inputs(cfg)
         if cfg.latent_dtype == "int4":
-            ck, sk = O.quantize_int4(inp["hk"])
-            cv, sv = O.quantize_int4(inp["hv"])
-            self.hk = O.dequant_int4(O.pack_int4(ck), sk).astype(np.float32)
-            self.hv = O.dequant_int4(O.pack_int4(cv), sv).astype(np.float32)
+            ck, sk = O.quantize_int4(hk)
+            cv, sv = O.quantize_int4(hv)
+            hk = O.dequant_int4(O.pack_int4(ck), sk)
+            hv = O.dequant_int4(O.pack_int4(cv), sv)
         else:
-            self.hk = gen.storage_round(inp["hk"], cfg.latent_dtype).float().numpy()
-            self.hv = gen.storage_round(inp["hv"], cfg.latent_dtype).float().numpy()
-        self.q = gen.storage_round(inp["q"], cfg.q_dtype).double().numpy()
-        self.bk = gen.storage_round(inp["bk"], cfg.bk_dtype).double().numpy()
-        self.seq = np.full(cfg.batch, cfg.T)
-        self.heads = [(b, i) for b in range(cfg.batch) for i in range(cfg.n_heads)]
+            hk = gen.storage_round(hk, cfg.latent_dtype).double().numpy()
+            hv = gen.storage_round(hv, cfg.latent_dtype).double().numpy()
+        s = cfg.group_size
+        self.hk = np.ascontiguousarray(hk[None, :, None, :])    # [1][T][1][r]
+        self.hv = np.ascontiguousarray(hv[None, :, None, :])
+        self.q = gen.storage_round(q[:1, :s], cfg.q_dtype).double().numpy()
+        self.bk = bk.double().numpy()[:1]                        # storage-rounded torch tensor
+        self.seq = np.array([cfg.T])
+        self.heads = [(0, j) for j in range(s)]
+        self.results = {}
 
-    def run(self, heads):
+    def run(self, head):
         c = self.cfg
-        return self.O.decode(self.q, self.hk, self.hv, self.bk, self.seq, c.group_size, mode=c.mode, theta=c.theta,
-                             heads=heads)
+        o, lse = self.O.decode(self.q, self.hk, self.hv, self.bk, self.seq, c.group_size, mode=c.mode,
+                               theta=c.theta, heads=[head])
+        self.results[head] = (o[head], lse[head])
+
+    def compare(self, gpu_out):
+        """max |GPU - oracle| over the heads the oracle has computed (batch row 0, group 0)."""
+        if not self.results:
+            return None
+        d = max(float(self.np.abs(gpu_out[0, j] - o).max()) for (_, j), (o, _) in self.results.items())
+        ref = max(float(self.np.abs(o).max()) for o, _ in self.results.values())
+        return {"heads": len(self.results), "max_abs_err": d, "max_err_over_max_ref": d / ref if ref else d}
 
 
-def cpu_baseline(cfg, work, budget_s=12.0):
+def cpu_baseline(sample, work, budget_s=12.0):
     """Time the oracle as it stands on this host's cores over a bounded sample of the workload."""
-    sample = OracleSample(cfg)
+    cfg = sample.cfg
+    total_heads = cfg.batch * cfg.n_heads
     done = 0
     t0 = time.perf_counter()
-    while time.perf_counter() - t0 < budget_s:
-        h = sample.heads[done % len(sample.heads)]
-        sample.run([h])
+    while time.perf_counter() - t0 < budget_s or done == 0:
+        sample.run(sample.heads[done % len(sample.heads)])
         done += 1
     el = time.perf_counter() - t0
-    frac = done / len(sample.heads)
+    frac = done / total_heads
     return {"value": round(work["decode_bytes"] * frac / el / 1e9, 4), "unit": "GB/s", "cores": _blas_threads(),
             "kind": "oracle", "seconds": round(el, 2),
-            "sample": f"{done} single-head decodes cycling over the workload's {len(sample.heads)} (batch, head) "
-                      f"pairs, all {cfg.T} tokens each, float64 NumPy"}
+            "sample": f"{done} single-head decodes (the {len(sample.heads)} heads of batch row 0, group 0, "
+                      f"cycled) of the workload's {total_heads}, all {cfg.T} tokens each, float64 NumPy"}
+
+
+def single_core_oracle(sample, work, budget_s):
+    """The same oracle sample on one core: a child process pinned to one CPU with BLAS threads
+    set to 1 before NumPy loads."""
+    import numpy as np
+    cfg = sample.cfg
+    with tempfile.TemporaryDirectory() as d:
+        path = os.path.join(d, "sample.npz")
+        np.savez(path, q=sample.q, hk=sample.hk, hv=sample.hv, bk=sample.bk, seq=sample.seq)
+        env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+        cmd = [sys.executable, os.path.abspath(__file__), "--oracle-child", path, "--oracle-child-cfg",
+               json.dumps({"group_size": cfg.group_size, "mode": cfg.mode, "theta": cfg.theta}),
+               "--cpu-seconds", str(budget_s)]
+        res = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=budget_s * 10 + 120)
+        if res.returncode != 0:
+            return {"error": res.stderr.strip().splitlines()[-1:] or ["child failed"]}
+        child = json.loads(res.stdout.strip().splitlines()[-1])
+    frac = child["heads"] / (cfg.batch * cfg.n_heads)
+    return {"value": round(work["decode_bytes"] * frac / child["seconds"] / 1e9, 4), "unit": "GB/s", "cores": 1,
+            "ms_per_head": round(child["seconds"] / child["heads"] * 1e3, 2),
+            "ms_per_step_equivalent": round(child["seconds"] / frac * 1e3, 1), "kind": "oracle"}
+
+
+def oracle_child(path, cfg_json, budget_s):
+    os.sched_setaffinity(0, {sorted(os.sched_getaffinity(0))[0]})
+    import numpy as np
+    from oracle import palu_oracle as O
+    c = json.loads(cfg_json)
+    z = np.load(path)
+    heads = [(0, j) for j in range(z["q"].shape[1])]
+    done = 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < budget_s or done == 0:
+        O.decode(z["q"], z["hk"], z["hv"], z["bk"], z["seq"], c["group_size"], mode=c["mode"], theta=c["theta"],
+                 heads=[heads[done % len(heads)]])
+        done += 1
+    print(json.dumps({"heads": done, "seconds": time.perf_counter() - t0}))
 
 
 def run_reference(args, cfg, name):
     world, rank, _ = _dist()
     if rank != 0:
         return None
+    import numpy as np
+    from synthetic import gen
     work = step_work(cfg)
-    sample = OracleSample(cfg)
-    per_step = sample.heads[:cfg.group_size]  # one G-LRD group of one batch row, all T tokens
-    frac = len(per_step) / len(sample.heads)
-    for _ in range(args.warmup):
-        sample.run(per_step)
+    fac, _ = gen.factors(cfg)
+    sample = OracleSample(cfg, gen.sample_group_latents(cfg, "k"), gen.sample_group_latents(cfg, "v"),
+                          gen.draw_query(cfg), gen.storage_round(fac["k"][1], cfg.bk_dtype))
+    # one head per step over all T tokens, cycling through the heads of batch row 0, group 0
+    frac = 1 / (cfg.batch * cfg.n_heads)
+    for i in range(args.warmup):
+        sample.run(sample.heads[i % len(sample.heads)])
     t0 = time.perf_counter()
-    for _ in range(args.steps):
-        sample.run(per_step)
+    for i in range(args.steps):
+        sample.run(sample.heads[i % len(sample.heads)])
     el = time.perf_counter() - t0
     ms = el / args.steps * 1e3
     val = round(work["decode_bytes"] * frac / (ms / 1e3) / 1e9, 4)
-    desc = f"{len(per_step)} heads (one group, batch row 0) of the workload per step, float64 NumPy"
+    desc = (f"one head per step (cycling over the {len(sample.heads)} heads of batch row 0, group 0) of the "
+            f"workload's {cfg.batch * cfg.n_heads}, all {cfg.T} tokens, float64 NumPy")
     return {"metric": METRIC, "value": val, "unit": "GB/s", "impl": "reference", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -487,24 +702,26 @@ def run_reference(args, cfg, name):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-per-config", action="store_true", help="time the headline workload only")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--per-config-steps", type=int, default=100, help="timed steps per workload above T=4K")
+    ap.add_argument("--per-config-cpu-seconds", type=float, default=3.0)
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch (profiling runs)")
     ap.add_argument("--tokens", type=int, default=None, help="override the workload's T (profiling runs)")
+    ap.add_argument("--oracle-child", default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--oracle-child-cfg", default=None, help=argparse.SUPPRESS)
     args = ap.parse_args(argv)
+    if args.oracle_child:
+        oracle_child(args.oracle_child, args.oracle_child_cfg, args.cpu_seconds)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    from synthetic import gen
-    base, T = WORKLOADS[args.workload]
-    cfg = getattr(gen, base) if T is None else getattr(gen, base).with_(T=T)
-    if args.batch is not None:
-        cfg = cfg.with_(batch=args.batch)
-    if args.tokens is not None:
-        cfg = cfg.with_(T=args.tokens)
+    cfg = config_of(args.workload, args.batch, args.tokens)
     res = run_reference(args, cfg, args.workload) if args.impl == "reference" else run_gpu(args, cfg, args.workload)
     if res is not None:
         print(json.dumps(res), flush=True)

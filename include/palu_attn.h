@@ -65,7 +65,9 @@ typedef struct CUstream_st* palu_stream_t;
 typedef enum palu_status_t {
   PALU_OK = 0,
   PALU_ERR_INVALID_ARG = 1,  /* null / misaligned pointer, bad size, inconsistent descriptor */
-  PALU_ERR_UNSUPPORTED = 2,  /* a valid shape or dtype combination this build has no kernel for */
+  PALU_ERR_UNSUPPORTED = 2,  /* a valid shape or dtype combination this build has no kernel for
+                                (shapes the descriptor accepts but no fast kernel covers are not
+                                refused: they run on the CUDA-core kernel, see palu_decode_plan) */
   PALU_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
   PALU_ERR_DEVICE = 4,       /* a kernel recorded an out-of-range index in the error word */
   PALU_ERR_TIMEOUT = 5,      /* a bounded device-side wait gave up (error word) */
@@ -177,7 +179,12 @@ palu_status_t palu_append_latents(palu_attn_t h, const palu_cache* cache, const 
  *   lse        device [batch][n_heads] float32 natural log-sum-exp of the scaled
  *              scores, or NULL. An empty row (seq_lens[b] == 0) yields o = 0 and
  *              lse = -inf.
- * Asynchronous on `stream`.
+ * Asynchronous on `stream`. Kernel choice: RoPE mode with fp16/bf16/int4 latents,
+ * head_dim 128, rank 256 and an even group size runs the tensor-core rebuild kernel;
+ * absorbed mode with fp16/bf16 latents, group size 4 and rank 256 runs the TMA
+ * streaming kernel; every other accepted descriptor (fp32 latents, int4 absorbed,
+ * group size 1, head_dim 64, ranks 64/128) runs the CUDA-core kernel, which is
+ * correct for all of them but not tuned. palu_decode_plan reports the choice.
  */
 palu_status_t palu_decode_attn(palu_attn_t h, const void* q, const palu_cache* cache,
                                const int32_t* seq_lens, const int32_t* positions, const int32_t* q_pos,
@@ -218,8 +225,12 @@ palu_status_t palu_decode_plan(palu_attn_t h, int64_t cache_capacity, int batch,
  *   - A request whose scratch (4 bytes x batch x n_heads x (rank_k + rank_v) for
  *     one split, plus alignment) does not fit in 8 MiB returns PALU_ERR_WORKSPACE
  *     before anything is queued; larger T only lowers the split count.
- *   - The first call on a device looks up the array's address on that device
- *     (cudaGetSymbolAddress), so make that first call before any stream capture.
+ *   - The device is the calling thread's current device, and `stream` must belong
+ *     to it (else PALU_ERR_INVALID_ARG). The first call on a device looks up the
+ *     array's address on that device (cudaGetSymbolAddress), so make that first
+ *     call before any stream capture.
+ *   - int4 latents need k_scale / v_scale as for palu_decode_attn (non-NULL, 2-byte
+ *     aligned, for each int4 side).
  *   - Every call shares the one array, and its contents persist between calls;
  *     the error word is cleared at the start of each call. Calls that overlap on
  *     the GPU (different streams, or host threads racing) race on the scratch:
@@ -229,6 +240,44 @@ palu_status_t palu_decode_plan(palu_attn_t h, int64_t cache_capacity, int batch,
 palu_status_t palu_decode_attn_noalloc(const palu_attn_desc* desc, const void* B_k, const void* q,
                                        const palu_cache* cache, const int32_t* seq_lens, int batch,
                                        int64_t max_seq_len, float* out, float* lse, palu_stream_t stream);
+
+/*
+ * The layer's output projection from the latent decode outputs, with B_v fused into
+ * W_o ("方法细节", value-fusion paragraph: head i's output p_i V_i = p_i H_v,g B_v^(i)
+ * only meets its own rows W_o^(i), so V is never rebuilt):
+ *   y[b] = sum_i o[b][i] W_f^(i),   W_f^(i) = B_v^(i) W_o^(i)   (rank_v x d_model).
+ *
+ * palu_fuse_value_output forms the fused weight once (an offline transform), on the
+ * current device:
+ *   B_v      device [n_g][rank_v][group_size * head_dim] in in_dtype (F32, F16, BF16),
+ *            the per-group value factor; head i uses column block i % s of group i / s
+ *   W_o      device [n_heads * head_dim][d_model] in in_dtype, row-major (the rows of
+ *            head i are i * head_dim .. (i + 1) * head_dim - 1)
+ *   W_fused  device [n_heads * rank_v][d_model] in out_dtype (F16 or BF16): head i's
+ *            block is rows i * rank_v .. (i + 1) * rank_v - 1; fp32 accumulation over
+ *            head_dim, rounded once to nearest
+ *
+ * palu_output_proj is the per-step GEMV y = o W_fused on the current device:
+ *   W_fused  device [k_dim][d_model] F16/BF16, 16-byte aligned; k_dim = n_heads * rank_v
+ *   o        device [batch][k_dim] float32 (palu_decode_attn's `out`, [batch][n][rank_v])
+ *   y        device [batch][d_model] float32, overwritten
+ *   workspace device, 256-byte aligned, palu_output_proj_workspace_size(k_dim, d_model,
+ *            max_batch) bytes for any batch <= max_batch; it must be zero-filled before
+ *            its first use, and every call leaves it ready for the next. Calls sharing a
+ *            workspace must not overlap on the GPU.
+ * d_model must be a multiple of 8 (else PALU_ERR_INVALID_ARG); k_dim <= 65536 and
+ * batch <= 1024 (else PALU_ERR_UNSUPPORTED). The result is deterministic (fixed
+ * summation order).
+ * `stream` must belong to the calling thread's current device (else
+ * PALU_ERR_INVALID_ARG). Asynchronous on `stream`.
+ */
+palu_status_t palu_fuse_value_output(const void* B_v, const void* W_o, palu_dtype_t in_dtype, int n_heads,
+                                     int head_dim, int group_size, int rank_v, int64_t d_model, void* W_fused,
+                                     palu_dtype_t out_dtype, palu_stream_t stream);
+palu_status_t palu_output_proj_workspace_size(int64_t k_dim, int64_t d_model, int max_batch, size_t* bytes);
+palu_status_t palu_output_proj(const void* W_fused, palu_dtype_t w_dtype, int64_t k_dim, int64_t d_model,
+                               const float* o, int batch, float* y, void* workspace, size_t workspace_bytes,
+                               palu_stream_t stream);
 
 /* Free the host handle. Does not synchronise: no work on it may be in flight. NULL is fine. */
 palu_status_t palu_destroy(palu_attn_t h);
@@ -248,18 +297,63 @@ palu_status_t palu_attn_check(palu_attn_t h, palu_stream_t stream);
 #define PALU_TRACE_CAPACITY 4096
 palu_status_t palu_attn_trace_enable(palu_attn_t h, int enable);
 palu_status_t palu_attn_trace_read(palu_attn_t h, int* launches, double* total_ms);
+/*
+ * Like palu_attn_trace_read, but writes each recorded launch's device time in
+ * milliseconds, in launch order, to ms[0 .. launches) (host memory, `capacity`
+ * entries; launches beyond it are dropped) and empties the ring.
+ */
+palu_status_t palu_attn_trace_times(palu_attn_t h, float* ms, int capacity, int* launches);
 
 /* Static description of a status code. */
 const char* palu_status_string(palu_status_t s);
 
 /*
- * Test hook for the int4 load path: writes, as float32, the dequantised latents
- * (code * scale) of tokens [0, n_tokens) of cache rows [0, batch) into
- * out [batch][n_tokens][n_g][rank] (device), using the same unpack routine the
- * decode kernels use. which = 0 for keys, 1 for values.
+ * Test hook for the int4 load path of the CUDA-core kernel (PALU_KERNEL_SIMT, which
+ * runs int4 absorbed decodes and the int4 shapes the tensor-core kernel does not
+ * take): writes, as float32, the dequantised latents (code * scale) of tokens
+ * [0, n_tokens) of cache rows [0, batch) into out [batch][n_tokens][n_g][rank]
+ * (device), with that kernel's unpack routine. which = 0 for keys, 1 for values.
+ * The tensor-core kernel unpacks with other routines; palu_debug_int4_operand and
+ * palu_debug_int4_dp2a export those.
  */
 palu_status_t palu_debug_dequant(palu_attn_t h, const palu_cache* cache, int which, int batch,
                                  int64_t n_tokens, float* out, palu_stream_t stream);
+
+/*
+ * Test hooks for the int4 path of the tensor-core RoPE kernel (PALU_KERNEL_TC_ROPE).
+ * They run that kernel's own device routines, so that a bit-exact comparison checks
+ * the code that decodes. The pages fix the stored format (per-token int4 latents,
+ * "补充细节" KV-quantisation paragraph; codes in [-7, 7]); the routines are this
+ * library's.
+ *
+ * palu_debug_int4_operand -- the key side. For every 128-token tile of rows [0, batch)
+ * it loads the packed key codes into shared memory with the decode kernel's TMA
+ * box and 128-byte swizzle, expands each token row with the decode kernel's
+ * converter into the swizzled fp16 tensor-core operand, reads the operand back and
+ * writes, for tokens [0, n_tokens):
+ *   codes  device [batch][n_tokens][n_g][rank_k] uint16: the fp16 bit pattern of each
+ *          operand element (the signed code as an exact fp16 number), in the operand's
+ *          rank order: within every run of eight consecutive ranks, position p holds
+ *          rank {0, 2, 4, 6, 1, 3, 5, 7}[p] (B_k^T is stored with the same order)
+ *   deq    device float, same shape and order: operand value x the token's key scale
+ *          (exact in fp32), or NULL
+ * Requires desc.k_dtype = PALU_INT4 and rank_k = 256 (else PALU_ERR_INVALID_ARG /
+ * PALU_ERR_UNSUPPORTED) and batch * capacity >= 128 (else PALU_ERR_UNSUPPORTED). A
+ * bounded wait that gives up is reported by palu_attn_check as PALU_ERR_TIMEOUT.
+ *
+ * palu_debug_int4_dp2a -- the value side (which = 1; which = 0 runs the same routine
+ * on the key codes). For every block of 16 tokens (tokens 16 k .. 16 k + 15 of
+ * [0, n_tokens), missing tokens counting as weight 0) and both heads h = 0, 1 of a
+ * head pair, the decode kernel's dp2a routine forms the exact integer sums
+ *   sums[b][k][g][h][c] = sum_t weights[b][t][h] * code[b][t][g][c]
+ * with weights device [batch][n_tokens][2] int32, each in [0, 32767] (the 15-bit
+ * weights the decode kernel feeds it; other values give undefined sums), and
+ * sums device [batch][ceil(n_tokens / 16)][n_g][2][rank] int32. Requires rank 256.
+ */
+palu_status_t palu_debug_int4_operand(palu_attn_t h, const palu_cache* cache, int batch, int64_t n_tokens,
+                                      uint16_t* codes, float* deq, palu_stream_t stream);
+palu_status_t palu_debug_int4_dp2a(palu_attn_t h, const palu_cache* cache, int which, int batch, int64_t n_tokens,
+                                   const int32_t* weights, int32_t* sums, palu_stream_t stream);
 
 #ifdef __cplusplus
 }

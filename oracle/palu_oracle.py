@@ -276,3 +276,37 @@ def dequant_int4(packed, scale) -> np.ndarray:
     """Latent value = code * scale, returned in float64 (exact)."""
     codes = unpack_int4(packed).astype(np.float64)
     return codes * np.asarray(scale, dtype=np.float16).astype(np.float64)[..., None]
+
+
+# ---------------------------------------------------------------------------
+# Value fusion into the output projection (the step after decode)
+# ---------------------------------------------------------------------------
+
+def fuse_value_output(bv, wo, group_size: int) -> np.ndarray:
+    """The fused matrices W_f^(i) = B_v^(i) W_o^(i) of every head i, stacked as
+    [n * r_v][d] ([Palu] "方法细节", value-fusion paragraph: head i's attention output
+    p_i V_i = p_i H_v,g B_v^(i) meets its rows of W_o, so B_v^(i) W_o^(i) can be
+    formed offline). B_v^(i) is column block j = i % s of group g = i // s of
+    bv [n_g][r_v][s*d_h]; W_o^(i) is rows i*d_h .. (i+1)*d_h - 1 of wo [n*d_h][d]."""
+    bv = np.asarray(bv, np.float64)
+    wo = np.asarray(wo, np.float64)
+    n_g, r_v, cols = bv.shape
+    d_h = cols // group_size
+    blocks = []
+    for i in range(n_g * group_size):
+        g, j = _group_of(i, group_size)
+        blocks.append(bv[g][:, j * d_h:(j + 1) * d_h] @ wo[i * d_h:(i + 1) * d_h])
+    return np.concatenate(blocks, axis=0)
+
+
+def project_fused(o, w_fused) -> np.ndarray:
+    """y[b] = sum_i o[b, i] W_f^(i): the layer output from the latent decode outputs
+    o [B][n][r_v], with W_f^(i) = rows i*r_v .. (i+1)*r_v - 1 of w_fused [n*r_v][d]."""
+    o = np.asarray(o, np.float64)
+    w = np.asarray(w_fused, np.float64)
+    B, n, r_v = o.shape
+    y = np.zeros((B, w.shape[1]))
+    for b in range(B):
+        for i in range(n):
+            y[b] += o[b, i] @ w[i * r_v:(i + 1) * r_v]
+    return y

@@ -154,6 +154,69 @@ __device__ __forceinline__ uint4 int4x8_to_half8(uint32_t w) {
   return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
+// The int4 key converter's work on one token row and one 64-rank chunk: packed bytes
+// 32 kc .. 32 kc + 31 of the row (16-byte chunks 2 kc and 2 kc + 1 of a tile loaded by TMA with
+// the 128-byte swizzle, row r) become 64 exact fp16 codes, written as row r of the 128-byte-
+// swizzled fp16 MMA operand chunk `arow` points into (arow = chunk base + 128 r).
+__device__ __forceinline__ void convert_int4_row_chunk(const uint8_t* prow, uint8_t* arow, int r, int kc) {
+  const uint4 w0 = *reinterpret_cast<const uint4*>(prow + (((2 * kc) ^ (r & 7)) << 4));
+  const uint4 w1 = *reinterpret_cast<const uint4*>(prow + (((2 * kc + 1) ^ (r & 7)) << 4));
+  const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+  for (int j = 0; j < 8; ++j) *reinterpret_cast<uint4*>(arow + ((j ^ (r & 7)) << 4)) = int4x8_to_half8(wv[j]);
+}
+
+// int4 p H_v on the raw value codes, per warp: 16 tokens (two groups of eight, ch = 0, 1) and two
+// heads. Lane l holds the 15-bit integer weight q of token l & 15 (group (l & 15) >> 3) for head
+// l >> 4; dp2a_pack_weights pairs neighbouring tokens' weights (valid in even lanes) and sums the
+// warp's weights per head.
+__device__ __forceinline__ void dp2a_pack_weights(uint32_t qv, uint32_t& qpair, uint32_t& qsum) {
+  qsum = qv;
+#pragma unroll
+  for (int o = 1; o < 16; o <<= 1) qsum += __shfl_xor_sync(0xffffffffu, qsum, o);
+  qpair = qv | (__shfl_down_sync(0xffffffffu, qv, 1) << 16);
+}
+
+// Accumulate sum_k q_k (code_k + 8) over the eight tokens of group ch for this lane's eight value
+// columns (8 lane .. 8 lane + 7) and both heads, exactly in int32. u[k] = the lane's four packed
+// bytes of token k of the group. dp2a multiplies two tokens' 16-bit weights by the two tokens'
+// biased codes of one column (one byte each).
+__device__ __forceinline__ void dp2a_accumulate8(const uint32_t (&u)[8], uint32_t qpair, int ch,
+                                                 uint32_t (&ai)[2][8]) {
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const uint32_t a0 = __shfl_sync(0xffffffffu, qpair, ch * 8 + 2 * m);
+    const uint32_t a1 = __shfl_sync(0xffffffffu, qpair, 16 + ch * 8 + 2 * m);
+    const uint32_t la = (u[2 * m] ^ 0x88888888u) & 0x0F0F0F0Fu;
+    const uint32_t lb = (u[2 * m + 1] ^ 0x88888888u) & 0x0F0F0F0Fu;
+    const uint32_t ha = ((u[2 * m] >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
+    const uint32_t hb = ((u[2 * m + 1] >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
+    const uint32_t b02 = __byte_perm(la, lb, 0x5140), b46 = __byte_perm(la, lb, 0x7362);
+    const uint32_t b13 = __byte_perm(ha, hb, 0x5140), b57 = __byte_perm(ha, hb, 0x7362);
+    ai[0][0] = dp2a_lo(a0, b02, ai[0][0]);
+    ai[0][2] = dp2a_hi(a0, b02, ai[0][2]);
+    ai[0][4] = dp2a_lo(a0, b46, ai[0][4]);
+    ai[0][6] = dp2a_hi(a0, b46, ai[0][6]);
+    ai[0][1] = dp2a_lo(a0, b13, ai[0][1]);
+    ai[0][3] = dp2a_hi(a0, b13, ai[0][3]);
+    ai[0][5] = dp2a_lo(a0, b57, ai[0][5]);
+    ai[0][7] = dp2a_hi(a0, b57, ai[0][7]);
+    ai[1][0] = dp2a_lo(a1, b02, ai[1][0]);
+    ai[1][2] = dp2a_hi(a1, b02, ai[1][2]);
+    ai[1][4] = dp2a_lo(a1, b46, ai[1][4]);
+    ai[1][6] = dp2a_hi(a1, b46, ai[1][6]);
+    ai[1][1] = dp2a_lo(a1, b13, ai[1][1]);
+    ai[1][3] = dp2a_hi(a1, b13, ai[1][3]);
+    ai[1][5] = dp2a_lo(a1, b57, ai[1][5]);
+    ai[1][7] = dp2a_hi(a1, b57, ai[1][7]);
+  }
+}
+
+// sum q code = sum q (code + 8) - 8 sum q, exact in int32 (|.| < 2^22)
+__device__ __forceinline__ int32_t dp2a_unbias(uint32_t acc, uint32_t qsum_head) {
+  return int32_t(acc - 8u * qsum_head);
+}
+
 // Fold the rotated query into B_k^T, in place, before the first MMA. B_k^T holds the head pair
 // interleaved (row 2 d + j = dimension d of head j). For head j and rotation pair k, rows
 // a = 2 k + j (dimension k) and b = a + 128 (dimension k + 64) become
@@ -662,10 +725,8 @@ __global__ void __launch_bounds__(Lay<I4>::kThreads, 1)
         for (int o = 1; o < 16; o <<= 1) smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o));
         const float inv = smax > 0.f ? 32767.f / smax : 0.f;
         const uint32_t qv = uint32_t(__float2int_rn(pw * inv));
-        uint32_t qsum = qv;
-#pragma unroll
-        for (int o = 1; o < 16; o <<= 1) qsum += __shfl_xor_sync(0xffffffffu, qsum, o);
-        const uint32_t qpair = qv | (__shfl_down_sync(0xffffffffu, qv, 1) << 16);  // valid in even lanes
+        uint32_t qsum, qpair;
+        dp2a_pack_weights(qv, qpair, qsum);
         uint32_t ai[2][8];
 #pragma unroll
         for (int c = 0; c < 8; ++c) ai[0][c] = ai[1][c] = 0u;
@@ -681,33 +742,7 @@ __global__ void __launch_bounds__(Lay<I4>::kThreads, 1)
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(&vempty[slot]);
           if (broken) continue;
-#pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            const uint32_t a0 = __shfl_sync(0xffffffffu, qpair, ch * 8 + 2 * m);
-            const uint32_t a1 = __shfl_sync(0xffffffffu, qpair, 16 + ch * 8 + 2 * m);
-            const uint32_t la = (u[2 * m] ^ 0x88888888u) & 0x0F0F0F0Fu;
-            const uint32_t lb = (u[2 * m + 1] ^ 0x88888888u) & 0x0F0F0F0Fu;
-            const uint32_t ha = ((u[2 * m] >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
-            const uint32_t hb = ((u[2 * m + 1] >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
-            const uint32_t b02 = __byte_perm(la, lb, 0x5140), b46 = __byte_perm(la, lb, 0x7362);
-            const uint32_t b13 = __byte_perm(ha, hb, 0x5140), b57 = __byte_perm(ha, hb, 0x7362);
-            ai[0][0] = dp2a_lo(a0, b02, ai[0][0]);
-            ai[0][2] = dp2a_hi(a0, b02, ai[0][2]);
-            ai[0][4] = dp2a_lo(a0, b46, ai[0][4]);
-            ai[0][6] = dp2a_hi(a0, b46, ai[0][6]);
-            ai[0][1] = dp2a_lo(a0, b13, ai[0][1]);
-            ai[0][3] = dp2a_hi(a0, b13, ai[0][3]);
-            ai[0][5] = dp2a_lo(a0, b57, ai[0][5]);
-            ai[0][7] = dp2a_hi(a0, b57, ai[0][7]);
-            ai[1][0] = dp2a_lo(a1, b02, ai[1][0]);
-            ai[1][2] = dp2a_hi(a1, b02, ai[1][2]);
-            ai[1][4] = dp2a_lo(a1, b46, ai[1][4]);
-            ai[1][6] = dp2a_hi(a1, b46, ai[1][6]);
-            ai[1][1] = dp2a_lo(a1, b13, ai[1][1]);
-            ai[1][3] = dp2a_hi(a1, b13, ai[1][3]);
-            ai[1][5] = dp2a_lo(a1, b57, ai[1][5]);
-            ai[1][7] = dp2a_hi(a1, b57, ai[1][7]);
-          }
+          dp2a_accumulate8(u, qpair, ch, ai);
         }
         if (!broken) {
           // back to float: sum(q * code) = sum(q * (code + 8)) - 8 sum(q), |.| < 2^22
@@ -716,8 +751,8 @@ __global__ void __launch_bounds__(Lay<I4>::kThreads, 1)
           const float sc1 = __shfl_sync(0xffffffffu, smax, 16) * (1.f / 32767.f);
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            const float2 v0 = make_float2(float(int32_t(ai[0][2 * c] - 8u * qs0)), float(int32_t(ai[0][2 * c + 1] - 8u * qs0)));
-            const float2 v1 = make_float2(float(int32_t(ai[1][2 * c] - 8u * qs1)), float(int32_t(ai[1][2 * c + 1] - 8u * qs1)));
+            const float2 v0 = make_float2(float(dp2a_unbias(ai[0][2 * c], qs0)), float(dp2a_unbias(ai[0][2 * c + 1], qs0)));
+            const float2 v1 = make_float2(float(dp2a_unbias(ai[1][2 * c], qs1)), float(dp2a_unbias(ai[1][2 * c + 1], qs1)));
             acc0[c] = __ffma2_rn(v0, make_float2(sc0, sc0), acc0[c]);
             acc1[c] = __ffma2_rn(v1, make_float2(sc1, sc1), acc1[c]);
           }
@@ -805,13 +840,7 @@ __global__ void __launch_bounds__(Lay<I4>::kThreads, 1)
             ok = false;
             break;
           }
-          // packed bytes 32 kc .. 32 kc + 31 of the row = 16-byte chunks 2 kc, 2 kc + 1 (swizzled)
-          const uint4 w0 = *reinterpret_cast<const uint4*>(prow + (((2 * kc) ^ (r & 7)) << 4));
-          const uint4 w1 = *reinterpret_cast<const uint4*>(prow + (((2 * kc + 1) ^ (r & 7)) << 4));
-          const uint32_t wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-          uint8_t* arow = smem + LY::kOffA + stage * kAStage + r * 128;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) *reinterpret_cast<uint4*>(arow + ((j ^ (r & 7)) << 4)) = int4x8_to_half8(wv[j]);
+          convert_int4_row_chunk(prow, smem + LY::kOffA + stage * kAStage + r * 128, r, kc);
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor cores
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(&fullA[stage]);
@@ -927,6 +956,142 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st) {
   if (i4) return launch_variant<Int4, true, true>(tm_hk, tm_hv, tm_b, P, st);
   if (a.k_dtype == kBF16) return launch_variant<__nv_bfloat16, false, false>(tm_hk, tm_hv, tm_b, P, st);
   return launch_variant<__half, false, true>(tm_hk, tm_hv, tm_b, P, st);
+}
+
+// ---------------------------------------------------------------------------- int4 test exports
+// Both kernels below run the int4 routines of decode_tc_kernel<Int4> itself (the same device
+// functions), so that their outputs can be compared bit for bit with the oracle.
+
+namespace {
+
+constexpr int kDbgPk = 0;                        // packed tile (128 tokens x 128 B), 1024-aligned
+constexpr int kDbgOp = kTile * (kRank / 2);      // fp16 operand: kChunks x 16 KB
+constexpr int kDbgBar = kDbgOp + kChunks * kAStage;
+constexpr int kDbgSmem = kDbgBar + 16 + 1024;
+
+// Key side: TMA loads a packed 128-token tile with the 128-byte swizzle, exactly as the decode
+// kernel's producer does; thread r converts row r with the converter routine into the swizzled
+// fp16 operand layout and reads its own row back, writing the operand values in the operand's
+// rank order and, in fp32, operand value x key scale.
+__global__ void __launch_bounds__(kTile) debug_int4_operand_kernel(const __grid_constant__ CUtensorMap tm_hk,
+                                                                   const __half* k_scale, int64_t capacity, int n_g,
+                                                                   int64_t n_tokens, uint16_t* codes, float* deq,
+                                                                   ErrWord* err, uint64_t wait_ns) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kDbgBar);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kDbgBar + 8);
+  const int r = threadIdx.x;
+  const int t0 = blockIdx.x * kTile, g = blockIdx.y, b = blockIdx.z;
+  if (r == 0) {
+    tc::mbar_init(bar, 1);
+    *abort_flag = 0;
+    tc::fence_barrier_init();
+  }
+  __syncthreads();
+  if (r == 0) {
+    tc::mbar_arrive_expect_tx(bar, kTile * (kRank / 2));
+    tc::tma_load_3d(smem + kDbgPk, &tm_hk, bar, 0, g, int(b * capacity + t0));
+  }
+  if (!tc::mbar_wait_bounded(bar, 0, abort_flag, wait_ns)) {
+    volatile int quiet = 0;
+    tc::mbar_wait_bounded(bar, 0, &quiet, wait_ns);   // the copy may still land: let it
+    if (r == 0) record_error(err, kCodeTimeout, kErrWait, blockIdx.x, b);
+    return;
+  }
+  uint8_t* arow_base = smem + kDbgOp + r * 128;
+  for (int kc = 0; kc < kChunks; ++kc) convert_int4_row_chunk(smem + kDbgPk + r * 128, arow_base + kc * kAStage, r, kc);
+  const int64_t t = t0 + r;
+  if (t >= n_tokens) return;
+  const float s = __half2float(k_scale[((int64_t)b * capacity + t) * n_g + g]);
+  const int64_t o = (((int64_t)b * n_tokens + t) * n_g + g) * kRank;
+  for (int kc = 0; kc < kChunks; ++kc) {
+    for (int j = 0; j < 8; ++j) {
+      const uint4 v = *reinterpret_cast<const uint4*>(arow_base + kc * kAStage + ((j ^ (r & 7)) << 4));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      const int64_t c0 = o + kc * kKChunk + j * 8;
+      for (int e = 0; e < 8; ++e) {
+        const uint16_t bits = uint16_t(w[e >> 1] >> (16 * (e & 1)));
+        codes[c0 + e] = bits;
+        if (deq) deq[c0 + e] = __half2float(__ushort_as_half(bits)) * s;
+      }
+    }
+  }
+}
+
+// Value side: one warp per (16-token block, group, batch row) runs the dp2a routine of the decode
+// kernel's p H_v over the block with the caller's 15-bit integer weights, and writes the exact
+// int32 sums sum_t w[t][head] code[t][c] for both heads.
+__global__ void debug_int4_dp2a_kernel(const uint8_t* cache, int64_t capacity, int n_g, int64_t n_tokens,
+                                       const int32_t* weights, int32_t* sums) {
+  const int lane = threadIdx.x & 31;
+  const int64_t blk = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  const int g = blockIdx.y, b = blockIdx.z;
+  const int64_t nblk = (n_tokens + 15) / 16;
+  if (blk >= nblk) return;   // warp-uniform
+  const int jt = lane & 15, hh = lane >> 4;
+  const int64_t tq = blk * 16 + jt;
+  const uint32_t qv = tq < n_tokens ? uint32_t(weights[((int64_t)b * n_tokens + tq) * 2 + hh]) : 0u;
+  uint32_t qpair, qsum;
+  dp2a_pack_weights(qv, qpair, qsum);
+  uint32_t ai[2][8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) ai[0][c] = ai[1][c] = 0u;
+  for (int ch = 0; ch < 2; ++ch) {
+    uint32_t u[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int64_t t = blk * 16 + ch * 8 + k;
+      u[k] = t < n_tokens
+                 ? *reinterpret_cast<const uint32_t*>(cache + (((int64_t)b * capacity + t) * n_g + g) * (kRank / 2) +
+                                                      lane * 4)
+                 : 0u;
+    }
+    dp2a_accumulate8(u, qpair, ch, ai);
+  }
+  const uint32_t qs0 = __shfl_sync(0xffffffffu, qsum, 0), qs1 = __shfl_sync(0xffffffffu, qsum, 16);
+  int32_t* o = sums + ((((int64_t)b * nblk + blk) * n_g + g) * 2) * kRank + lane * 8;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    o[c] = dp2a_unbias(ai[0][c], qs0);
+    o[kRank + c] = dp2a_unbias(ai[1][c], qs1);
+  }
+}
+
+}  // namespace
+
+bool tc_int4_debug_supported(int n_g, int rank, int64_t rows) {
+  return rank == kRank && n_g > 0 && rows >= kTile && rows < (int64_t(1) << 31) && encode_fn() != nullptr;
+}
+
+cudaError_t launch_debug_int4_operand(const void* hk, const __half* k_scale, int64_t capacity, int n_g, int batch,
+                                      int64_t n_tokens, uint16_t* codes, float* deq, ErrWord* err,
+                                      cudaStream_t st) {
+  if (!tc_int4_debug_supported(n_g, kRank, (int64_t)batch * capacity)) return cudaErrorNotSupported;
+  if (n_tokens == 0 || batch == 0) return cudaSuccess;
+  CUtensorMap tm;
+  const cuuint64_t dims[3] = {(cuuint64_t)kRank / 2, (cuuint64_t)n_g, (cuuint64_t)batch * capacity};
+  const cuuint64_t strides[2] = {(cuuint64_t)kRank / 2, (cuuint64_t)n_g * (kRank / 2)};
+  const cuuint32_t box[3] = {kRank / 2, 1, kTile};   // the decode kernel's H_k box and swizzle
+  if (!encode(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, hk, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(debug_int4_operand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDbgSmem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)((n_tokens + kTile - 1) / kTile), (unsigned)n_g, (unsigned)batch);
+  debug_int4_operand_kernel<<<grid, kTile, kDbgSmem, st>>>(tm, k_scale, capacity, n_g, n_tokens, codes, deq, err,
+                                                          1000000000ull);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_debug_int4_dp2a(const void* cache, int64_t capacity, int n_g, int batch, int64_t n_tokens,
+                                   const int32_t* weights, int32_t* sums, cudaStream_t st) {
+  if (n_tokens == 0 || batch == 0) return cudaSuccess;
+  const int64_t nblk = (n_tokens + 15) / 16;
+  const int warps = 4;
+  dim3 grid((unsigned)((nblk + warps - 1) / warps), (unsigned)n_g, (unsigned)batch);
+  debug_int4_dp2a_kernel<<<grid, warps * 32, 0, st>>>(static_cast<const uint8_t*>(cache), capacity, n_g, n_tokens,
+                                                      weights, sums);
+  return cudaGetLastError();
 }
 
 }  // namespace palu

@@ -78,6 +78,12 @@ bool tc_supported(const DecodeArgs& a);
 int tc_tile_tokens();
 int tc_ctas_per_group(const DecodeArgs& a);
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st);
+// int4 test exports that run the tensor-core kernel's own converter and dp2a routines
+bool tc_int4_debug_supported(int n_g, int rank, int64_t rows);
+cudaError_t launch_debug_int4_operand(const void* hk, const __half* k_scale, int64_t capacity, int n_g, int batch,
+                                      int64_t n_tokens, uint16_t* codes, float* deq, ErrWord* err, cudaStream_t st);
+cudaError_t launch_debug_int4_dp2a(const void* cache, int64_t capacity, int n_g, int batch, int64_t n_tokens,
+                                   const int32_t* weights, int32_t* sums, cudaStream_t st);
 
 // TMA-streaming absorbed-mode kernel (decode_abs.cu)
 bool abs_supported(const DecodeArgs& a);

@@ -60,7 +60,8 @@ extern "C" palu_status_t palu_decode_attn_noalloc(const palu_attn_desc* desc, co
     return PALU_ERR_INVALID_ARG;
   if (!cache || !cache->hk || !cache->hv || cache->capacity <= 0) return PALU_ERR_INVALID_ARG;
   if ((uintptr_t)cache->hk % 16 || (uintptr_t)cache->hv % 16) return PALU_ERR_INVALID_ARG;
-  if (desc->k_dtype == PALU_INT4 && (!cache->k_scale || !cache->v_scale)) return PALU_ERR_INVALID_ARG;
+  if (desc->k_dtype == PALU_INT4 && (!cache->k_scale || (uintptr_t)cache->k_scale % 2)) return PALU_ERR_INVALID_ARG;
+  if (desc->v_dtype == PALU_INT4 && (!cache->v_scale || (uintptr_t)cache->v_scale % 2)) return PALU_ERR_INVALID_ARG;
   if (max_seq_len < 0 || max_seq_len > desc->max_tokens || max_seq_len > cache->capacity)
     return PALU_ERR_INVALID_ARG;
 
@@ -70,8 +71,15 @@ extern "C" palu_status_t palu_decode_attn_noalloc(const palu_attn_desc* desc, co
   const size_t per_split = bh * desc->rank_v * sizeof(float) + bh * sizeof(float2);
   if (fixed + per_split + 512 > kNoAllocScratchBytes) return PALU_ERR_WORKSPACE;  // beyond the fixed scratch
 
-  int dev = 0;
+  // the scratch address is per device: the stream must belong to the current device
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int dev = 0, stream_dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PALU_ERR_CUDA;
+  if (cudaStreamGetDevice(s, &stream_dev) != cudaSuccess) {
+    cudaGetLastError();
+    return PALU_ERR_INVALID_ARG;
+  }
+  if (stream_dev != dev) return PALU_ERR_INVALID_ARG;
   char* scratch = nullptr;
   int sms = 0;
   st = scratch_for(dev, &scratch, &sms);
@@ -120,7 +128,6 @@ extern "C" palu_status_t palu_decode_attn_noalloc(const palu_attn_desc* desc, co
   a.n_splits = (int)splits;
   a.tiles_per_split = (int)tps;
 
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const float qscale = float(1.4426950408889634 / sqrt((double)desc->head_dim));
   cudaError_t e = cudaMemsetAsync(scratch, 0, 256, s);  // the error word starts at zero on every call
   if (e == cudaSuccess) e = launch_qprep(kAbsorbed, q, (int)desc->q_dtype, a, nullptr, qscale, qbuf, s);

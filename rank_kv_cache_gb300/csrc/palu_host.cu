@@ -243,6 +243,19 @@ palu_status_t palu_attn_trace_read(palu_attn_t h, int* launches, double* total_m
   return PALU_OK;
 }
 
+palu_status_t palu_attn_trace_times(palu_attn_t h, float* ms, int capacity, int* launches) {
+  if (!h || !launches || capacity < 0 || (capacity > 0 && !ms)) return PALU_ERR_INVALID_ARG;
+  if (cudaSetDevice(h->device) != cudaSuccess) return PALU_ERR_CUDA;
+  const int n = h->trace.n < capacity ? h->trace.n : capacity;
+  for (int i = 0; i < n; ++i) {
+    if (cudaEventSynchronize(h->trace.ev[2 * i + 1]) != cudaSuccess) return PALU_ERR_CUDA;
+    if (cudaEventElapsedTime(&ms[i], h->trace.ev[2 * i], h->trace.ev[2 * i + 1]) != cudaSuccess) return PALU_ERR_CUDA;
+  }
+  *launches = n;
+  h->trace.n = 0;
+  return PALU_OK;
+}
+
 // Event pair for the next traced launch, or nullptr when tracing is off or the ring is full.
 static cudaEvent_t* trace_slot(palu_attn* h) {
   Trace& t = h->trace;
@@ -423,6 +436,41 @@ palu_status_t palu_debug_dequant(palu_attn_t h, const palu_cache* cache, int whi
                                              to_dt(dt), cache->capacity, h->n_g,
                                              which == 0 ? h->d.rank_k : h->d.rank_v, batch, n_tokens, out,
                                              reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PALU_OK : PALU_ERR_CUDA;
+}
+
+palu_status_t palu_debug_int4_operand(palu_attn_t h, const palu_cache* cache, int batch, int64_t n_tokens,
+                                      uint16_t* codes, float* deq, palu_stream_t stream) {
+  if (!h || !codes || (uintptr_t)codes % 2 || (uintptr_t)deq % 4) return PALU_ERR_INVALID_ARG;
+  palu_status_t st = check_cache(h, cache);
+  if (st != PALU_OK) return st;
+  if (h->d.k_dtype != PALU_INT4) return PALU_ERR_INVALID_ARG;
+  if (batch < 0 || batch > h->d.max_batch || n_tokens < 0 || n_tokens > cache->capacity) return PALU_ERR_INVALID_ARG;
+  if (batch == 0 || n_tokens == 0) return PALU_OK;
+  if (!tc_int4_debug_supported(h->n_g, h->d.rank_k, (int64_t)batch * cache->capacity)) return PALU_ERR_UNSUPPORTED;
+  if (cudaSetDevice(h->device) != cudaSuccess) return PALU_ERR_CUDA;
+  const cudaError_t e = launch_debug_int4_operand(cache->hk, static_cast<const __half*>(cache->k_scale),
+                                                  cache->capacity, h->n_g, batch, n_tokens, codes, deq,
+                                                  reinterpret_cast<ErrWord*>(h->ws + h->L.err),
+                                                  reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PALU_OK : PALU_ERR_CUDA;
+}
+
+palu_status_t palu_debug_int4_dp2a(palu_attn_t h, const palu_cache* cache, int which, int batch, int64_t n_tokens,
+                                   const int32_t* weights, int32_t* sums, palu_stream_t stream) {
+  if (!h || (which != 0 && which != 1)) return PALU_ERR_INVALID_ARG;
+  palu_status_t st = check_cache(h, cache);
+  if (st != PALU_OK) return st;
+  const palu_dtype_t dt = which == 0 ? h->d.k_dtype : h->d.v_dtype;
+  const int rank = which == 0 ? h->d.rank_k : h->d.rank_v;
+  if (dt != PALU_INT4) return PALU_ERR_INVALID_ARG;
+  if (batch < 0 || batch > h->d.max_batch || n_tokens < 0 || n_tokens > cache->capacity) return PALU_ERR_INVALID_ARG;
+  if (batch == 0 || n_tokens == 0) return PALU_OK;
+  if (!weights || !sums || (uintptr_t)weights % 4 || (uintptr_t)sums % 4) return PALU_ERR_INVALID_ARG;
+  if (rank != 256) return PALU_ERR_UNSUPPORTED;
+  if (cudaSetDevice(h->device) != cudaSuccess) return PALU_ERR_CUDA;
+  const cudaError_t e = launch_debug_int4_dp2a(which == 0 ? cache->hk : cache->hv, cache->capacity, h->n_g, batch,
+                                               n_tokens, weights, sums, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PALU_OK : PALU_ERR_CUDA;
 }
 

@@ -314,7 +314,8 @@ cudaError_t launch_append(void* cache_k, __half* scale_k, int rank_k, const void
 }
 
 // ---------------------------------------------------------------------------
-// Debug export of dequantised int4 latents through the decode kernels' unpack routine.
+// Debug export of dequantised int4 latents through the CUDA-core decode kernel's unpack routine
+// (Latent<Int4>::get); the tensor-core kernel's routines have their own exports in decode_tc.cu.
 // ---------------------------------------------------------------------------
 __global__ void debug_dequant_kernel(const void* cache, const __half* scale, int64_t capacity, int n_g, int rank,
                                      int batch, int64_t n_tokens, float* out) {

@@ -31,7 +31,9 @@ MODES = {"rope": PALU_MODE_ROPE, "absorbed": PALU_MODE_ABSORBED}
 # every symbol include/palu_attn.h declares
 EXPORTS = ("palu_attn_workspace_size", "palu_attn_create", "palu_append_latents", "palu_decode_attn",
            "palu_destroy", "palu_attn_check", "palu_status_string", "palu_debug_dequant",
-           "palu_attn_trace_enable", "palu_attn_trace_read", "palu_decode_attn_noalloc", "palu_decode_plan")
+           "palu_attn_trace_enable", "palu_attn_trace_read", "palu_decode_attn_noalloc", "palu_decode_plan",
+           "palu_debug_int4_operand", "palu_debug_int4_dp2a", "palu_attn_trace_times",
+           "palu_fuse_value_output", "palu_output_proj_workspace_size", "palu_output_proj")
 PALU_TRACE_CAPACITY = 4096
 
 
@@ -74,6 +76,12 @@ def _load():
         "palu_decode_attn_noalloc": (I, [ctypes.POINTER(palu_attn_desc), P, P, ctypes.POINTER(palu_cache), P, I,
                                          I64, P, P, P]),
         "palu_decode_plan": (I, [P, I64, I, I64, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(I)]),
+        "palu_attn_trace_times": (I, [P, ctypes.POINTER(ctypes.c_float), I, ctypes.POINTER(I)]),
+        "palu_fuse_value_output": (I, [P, P, I, I, I, I, I, I64, P, I, P]),
+        "palu_output_proj_workspace_size": (I, [I64, I64, I, ctypes.POINTER(SZ)]),
+        "palu_output_proj": (I, [P, I, I64, I64, P, I, P, P, SZ, P]),
+        "palu_debug_int4_operand": (I, [P, ctypes.POINTER(palu_cache), I, I64, P, P, P]),
+        "palu_debug_int4_dp2a": (I, [P, ctypes.POINTER(palu_cache), I, I, I64, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -128,6 +136,15 @@ def palu_debug_dequant(h, cache: palu_cache, which: int, batch: int, n_tokens: i
     return _lib.palu_debug_dequant(h, ctypes.byref(cache), which, batch, n_tokens, out, stream)
 
 
+def palu_debug_int4_operand(h, cache: palu_cache, batch: int, n_tokens: int, codes: int, deq, stream: int) -> int:
+    return _lib.palu_debug_int4_operand(h, ctypes.byref(cache), batch, n_tokens, codes, deq, stream)
+
+
+def palu_debug_int4_dp2a(h, cache: palu_cache, which: int, batch: int, n_tokens: int, weights: int, sums: int,
+                         stream: int) -> int:
+    return _lib.palu_debug_int4_dp2a(h, ctypes.byref(cache), which, batch, n_tokens, weights, sums, stream)
+
+
 def palu_attn_trace_enable(h, enable: int) -> int:
     return _lib.palu_attn_trace_enable(h, int(enable))
 
@@ -137,6 +154,14 @@ def palu_attn_trace_read(h):
     ms = ctypes.c_double(0.0)
     st = _lib.palu_attn_trace_read(h, ctypes.byref(n), ctypes.byref(ms))
     return st, n.value, ms.value
+
+
+def palu_attn_trace_times(h, capacity: int = PALU_TRACE_CAPACITY):
+    """(status, [ms per recorded launch]) and empties the trace ring."""
+    buf = (ctypes.c_float * max(capacity, 1))()
+    n = ctypes.c_int(0)
+    st = _lib.palu_attn_trace_times(h, buf, capacity, ctypes.byref(n))
+    return st, [float(buf[i]) for i in range(n.value)]
 
 
 def palu_decode_attn_noalloc(desc: palu_attn_desc, bk: int, q: int, cache: palu_cache, seq_lens: int, batch: int,
@@ -152,6 +177,23 @@ def palu_decode_plan(h, cache_capacity: int, batch: int, max_seq_len: int):
     st = _lib.palu_decode_plan(h, cache_capacity, batch, max_seq_len, ctypes.byref(k), ctypes.byref(n),
                                ctypes.byref(l))
     return st, k.value, n.value, l.value
+
+
+def palu_fuse_value_output(bv: int, wo: int, in_dtype: int, n_heads: int, head_dim: int, group_size: int,
+                           rank_v: int, d_model: int, w_fused: int, out_dtype: int, stream: int) -> int:
+    return _lib.palu_fuse_value_output(bv, wo, in_dtype, n_heads, head_dim, group_size, rank_v, d_model, w_fused,
+                                       out_dtype, stream)
+
+
+def palu_output_proj_workspace_size(k_dim: int, d_model: int, max_batch: int):
+    n = ctypes.c_size_t(0)
+    st = _lib.palu_output_proj_workspace_size(k_dim, d_model, max_batch, ctypes.byref(n))
+    return st, n.value
+
+
+def palu_output_proj(w_fused: int, w_dtype: int, k_dim: int, d_model: int, o: int, batch: int, y: int,
+                     workspace: int, ws_bytes: int, stream: int) -> int:
+    return _lib.palu_output_proj(w_fused, w_dtype, k_dim, d_model, o, batch, y, workspace, ws_bytes, stream)
 
 
 def check(status: int, what: str = "palu") -> None:
@@ -281,3 +323,44 @@ class PaluAttention:
 
     def check_device(self, stream=None):
         check(palu_attn_check(self.handle, _stream_handle(stream)), "palu_attn_check")
+
+
+class OutputProjection:
+    """The fused (B_v W_o) weight of one layer and the workspace of its GEMV."""
+
+    def __init__(self, bv, wo, *, n_heads, head_dim, group_size, rank_v, max_batch=1, dtype="f16", stream=None):
+        torch = _torch()
+        _require_contiguous(bv=bv, wo=wo)
+        tmap = {torch.float32: PALU_F32, torch.float16: PALU_F16, torch.bfloat16: PALU_BF16}
+        if bv.dtype != wo.dtype:
+            raise ValueError("bv and wo must share a dtype")
+        self.d_model = int(wo.shape[1])
+        self.k_dim = n_heads * rank_v
+        self.w_dtype = DTYPES[dtype]
+        self.w = torch.empty((self.k_dim, self.d_model), dtype={"f16": torch.float16, "bf16": torch.bfloat16}[dtype],
+                             device=wo.device)
+        check(palu_fuse_value_output(_ptr(bv), _ptr(wo), tmap[bv.dtype], n_heads, head_dim, group_size, rank_v,
+                                     self.d_model, _ptr(self.w), self.w_dtype, _stream_handle(stream)),
+              "palu_fuse_value_output")
+        self._alloc_ws(max_batch, wo.device)
+
+    def _alloc_ws(self, max_batch, device):
+        torch = _torch()
+        st, n = palu_output_proj_workspace_size(self.k_dim, self.d_model, max_batch)
+        check(st, "palu_output_proj_workspace_size")
+        self.max_batch = max_batch
+        self.workspace = torch.zeros(n + 256, dtype=torch.uint8, device=device)
+        base = int(self.workspace.data_ptr())
+        self.ws_ptr, self.ws_bytes = base + (-base) % 256, n
+
+    def __call__(self, o, y=None, stream=None):
+        torch = _torch()
+        _require_contiguous(o=o, y=y)
+        B = o.shape[0]
+        if B > self.max_batch:
+            raise ValueError("batch larger than max_batch")
+        if y is None:
+            y = torch.empty((B, self.d_model), dtype=torch.float32, device=o.device)
+        check(palu_output_proj(_ptr(self.w), self.w_dtype, self.k_dim, self.d_model, _ptr(o), B, _ptr(y),
+                               self.ws_ptr, self.ws_bytes, _stream_handle(stream)), "palu_output_proj")
+        return y

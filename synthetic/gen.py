@@ -202,6 +202,54 @@ def make_inputs(cfg: Config, *, exact_x: bool | None = None, q_scale: float = 1.
     return out
 
 
+def draw_query(cfg: Config, q_scale: float = 1.0) -> np.ndarray:
+    """The workload's query alone, [B][n][d_h] float32: the same draw make_inputs returns."""
+    _, _, _, rq, _ = _streams(cfg.stream)
+    q = rq.standard_normal((cfg.batch, cfg.n_heads, cfg.head_dim), dtype=np.float32)
+    return q * np.float32(q_scale)
+
+
+def sample_group_latents(cfg: Config, which: str = "k", b: int = 0, g: int = 0) -> np.ndarray:
+    """[T][r] float32 latents of one (batch row, group), in the equivalent form
+    H = z sqrt(S_r) [R], from a seed stream of their own (keyed by side, b and g).
+    For CPU-side samples of a workload (timing the oracle) without drawing the
+    whole cache."""
+    fac, R = factors(cfg)
+    key = (1000, 0 if which == "k" else 1, b, g)
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence(SEED_BASE + cfg.stream, spawn_key=key)))
+    z = rng.standard_normal((cfg.T, cfg.rank), dtype=np.float32)
+    z *= np.sqrt(fac[which][2][g]).astype(np.float32)[None, :]
+    if R is not None:
+        z = z @ R.astype(np.float32)
+    return np.ascontiguousarray(z, dtype=np.float32)
+
+
+def latent_rows_torch(cfg: Config, device, which: str = "k"):
+    """Seeded latents drawn on a CUDA device, one batch row at a time (a generator of
+    [T][n_g][r] float32 tensors, batch row b = 0 .. B-1).
+
+    The draw is the equivalent form of H = x A used for large workloads,
+    H = z sqrt(S_r) [R] with z ~ N(0, I_r) (x U_r is exactly N(0, I_r)), taken with
+    torch's device generator seeded from SeedSequence(20261202 + stream) so that
+    multi-gigabyte caches are drawn in well under a second. The benchmark uses it;
+    the parity tests use make_inputs.
+    """
+    import torch
+    fac, R = factors(cfg)
+    seed = int(np.random.SeedSequence(SEED_BASE + cfg.stream).generate_state(1, np.uint64)[0] >> 1)
+    seed += 0 if which == "k" else 1
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    sq = torch.from_numpy(np.sqrt(fac[which][2]).astype(np.float32)).to(device)       # [n_g][r]
+    Rt = None if R is None else torch.from_numpy(R.astype(np.float32)).to(device)
+    for _ in range(cfg.batch):
+        z = torch.randn((cfg.T, cfg.n_groups, cfg.rank), generator=g, device=device, dtype=torch.float32)
+        z.mul_(sq[None])
+        if Rt is not None:
+            z = z @ Rt
+        yield z
+
+
 _TORCH_DT = {"f32": "float32", "f16": "float16", "bf16": "bfloat16"}
 
 

@@ -50,6 +50,44 @@ def test_rope_default_query_position_with_positions():
     assert_close(out, ref, lse, lse_ref)
 
 
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 127, 128, 129])
+@pytest.mark.parametrize("lat", ["f16", "bf16"])
+def test_absorbed_stage_edges(lat, T):
+    # the absorbed kernel streams 64-token stages, 8 tokens per warp: lengths at and around the
+    # stage edges, with a shorter second row
+    cfg = gen.ABSORBED_FP16.with_(T=T, batch=2, latent_dtype=lat)
+    c = Case(cfg, seq_lens=[T, max(1, T - 37)])
+    out, lse = c.run_gpu()
+    ref, lse_ref = c.run_oracle()
+    assert_close(out, ref, lse, lse_ref)
+
+
+@pytest.mark.parametrize("lat", ["f16", "bf16"])
+def test_absorbed_peaked_softmax_stress(lat):
+    cfg = gen.ABSORBED_FP16.with_(T=777, batch=2, latent_dtype=lat)
+    c = Case(cfg, seq_lens=[777, 300], q_scale=8.0)
+    out, lse = c.run_gpu()
+    ref, lse_ref = c.run_oracle()
+    assert_close(out, ref, lse, lse_ref)
+
+
+@pytest.mark.parametrize("T", [1, 2, 127, 128, 129, 1000])
+def test_rope_bf16_tile_edges(T):
+    cfg = gen.ROPE_BF16.with_(T=T, batch=2)
+    c = Case(cfg, seq_lens=[T, max(1, (T * 2) // 3)])
+    out, lse = c.run_gpu()
+    ref, lse_ref = c.run_oracle()
+    assert_close(out, ref, lse, lse_ref)
+
+
+def test_rope_bf16_peaked_softmax_stress():
+    cfg = gen.ROPE_BF16.with_(T=600, batch=2)
+    c = Case(cfg, seq_lens=[600, 257], q_scale=8.0)
+    out, lse = c.run_gpu()
+    ref, lse_ref = c.run_oracle()
+    assert_close(out, ref, lse, lse_ref)
+
+
 def test_absorbed_fp16_ragged():
     cfg = gen.ABSORBED_FP16.with_(T=1000, batch=2)
     c = Case(cfg, seq_lens=[1000, 333])

@@ -92,6 +92,27 @@ def _softmax_no_norm(scores, values):
     return e @ values, m + math.log(e.sum())
 
 
+def _fuse_wrong_head_block(bv, wo, group_size):
+    # every head of a group takes the group's first column block of B_v
+    bv, wo = np.asarray(bv, np.float64), np.asarray(wo, np.float64)
+    n_g, r_v, cols = bv.shape
+    d_h = cols // group_size
+    return np.concatenate([bv[i // group_size][:, :d_h] @ wo[i * d_h:(i + 1) * d_h]
+                           for i in range(n_g * group_size)], axis=0)
+
+
+def _project_rows_of_next_head(o, w_fused):
+    # off-by-one head: head i meets the rows of head (i + 1) % n
+    o, w = np.asarray(o, np.float64), np.asarray(w_fused, np.float64)
+    B, n, r_v = o.shape
+    y = np.zeros((B, w.shape[1]))
+    for b in range(B):
+        for i in range(n):
+            k = (i + 1) % n
+            y[b] += o[b, i] @ w[k * r_v:(k + 1) * r_v]
+    return y
+
+
 ALL_PINS = [getattr(P, n) for n in dir(P) if n.startswith("test_")]
 
 MUTATIONS = {
@@ -105,6 +126,8 @@ MUTATIONS = {
     "int4_nibble_order": ("pack_int4", _pack_swapped),
     "query_position_default": ("_query_position", _qpos_off_by_one),
     "softmax_unnormalised": ("softmax_attend", _softmax_no_norm),
+    "fuse_wrong_head_block": ("fuse_value_output", _fuse_wrong_head_block),
+    "project_rows_of_next_head": ("project_fused", _project_rows_of_next_head),
 }
 
 

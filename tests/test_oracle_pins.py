@@ -253,6 +253,46 @@ def test_value_fusion_into_output_projection():
     np.testing.assert_allclose(y, y_ref, atol=1e-11)
 
 
+def test_fused_output_projection_equals_uncompressed_mha_output_at_full_rank():
+    # At full rank r = s*d_h with exact SVD factors the latent path is the MHA layer itself, so
+    # sum_i o_i (B_v^(i) W_o^(i)) must equal concat_i(a_i) W_o of plain multi-head attention.
+    B, T, d, n, s, d_h = 2, 9, 32, 4, 2, 4
+    x, wk, wv, q = _mha_setup(21, B, T, d, n, s, d_h)
+    rng = np.random.default_rng(22)
+    wo = rng.standard_normal((n * d_h, d)) / math.sqrt(d)
+    n_g, r = n // s, s * d_h
+    Ak, Bk = _group_factors(wk, n_g, s, d_h, r)
+    Av, Bv = _group_factors(wv, n_g, s, d_h, r)
+    hk = np.einsum("btd,gdr->btgr", x, Ak)
+    hv = np.einsum("btd,gdr->btgr", x, Av)
+    o, _ = O.decode(q, hk, hv, Bk, [T, T - 3], s)
+    y = O.project_fused(o, O.fuse_value_output(Bv, wo, s))
+    a, _ = O.mha_decode(q, x, wk, wv, [T, T - 3])
+    y_ref = a.reshape(B, n * d_h) @ wo
+    np.testing.assert_allclose(y, y_ref, rtol=1e-10, atol=1e-11)
+
+
+def test_fused_output_projection_brute_force_tiny():
+    # scalar loops with exact summation, written from the definition y_c = sum_i sum_m o_im W_f,(i m) c
+    rng = np.random.default_rng(23)
+    n_g, s, d_h, r, d, B = 2, 2, 3, 2, 5, 2
+    bv = rng.standard_normal((n_g, r, s * d_h))
+    wo = rng.standard_normal((n_g * s * d_h, d))
+    o = rng.standard_normal((B, n_g * s, r))
+    wf = O.fuse_value_output(bv, wo, s)
+    for i in range(n_g * s):
+        g, j = i // s, i % s
+        for m in range(r):
+            for c in range(d):
+                want = math.fsum(bv[g, m, j * d_h + e] * wo[i * d_h + e, c] for e in range(d_h))
+                assert abs(wf[i * r + m, c] - want) < 1e-12
+    y = O.project_fused(o, wf)
+    for b in range(B):
+        for c in range(d):
+            want = math.fsum(o[b, i, m] * wf[i * r + m, c] for i in range(n_g * s) for m in range(r))
+            assert abs(y[b, c] - want) < 1e-12
+
+
 def test_absorbed_equals_rebuild_when_rotation_is_identity():
     # Key fusion: q K^T = (q B^T) H^T. With every position 0, RoPE is the identity.
     q, hk, hv, bk = _tiny(seed=9, B=2, T=8, n=4, s=2, d_h=4, r=4, r_v=3)
