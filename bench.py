@@ -493,6 +493,7 @@ def run_gpu(args, cfg, name):
     torch.cuda.empty_cache()
     if rank == 0 and world == 1 and not args.no_per_config:
         result["per_config"] = run_per_config(args, dev, flush, name, headline_entry, peaks, peaks_src)
+        result["next_rows"] = run_next_rows(args, dev, flush, peaks, peaks_src)
     if dist:
         dist.barrier()
         dist.destroy_process_group()
@@ -553,6 +554,94 @@ def run_per_config(args, dev, flush, headline, headline_entry, peaks, peaks_src)
               f"{e['roofline']['bound']} frac {e['roofline']['frac']}", file=sys.stderr, flush=True)
         wl.close()
         del wl
+        torch.cuda.empty_cache()
+    return out
+
+
+# ---------------------------------------------------------------------------
+# The steps around the decode: output projection (and the rows after it)
+# ---------------------------------------------------------------------------
+
+def event_times(fn, n, flush):
+    """n CUDA-event timings (ms) of fn() on the current stream, L2 flushed before each."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for i in range(n):
+        flush.zero_()
+        ev[i][0].record()
+        fn()
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def hbm_roofline(nbytes, ms, peaks, peaks_src):
+    ach = nbytes / (ms / 1e3) / 1e9
+    hbm = float(peaks["hbm_gbs"])
+    return {"bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s", "frac": round(ach / hbm, 4),
+            "roofline_us": round(nbytes / (hbm * 1e9) * 1e6, 2), "peak_source": f"hbm_gbs of {peaks_src}",
+            "duration": "median launch"}
+
+
+def oracle_seconds(fn, budget_s):
+    """(calls, seconds) of the oracle function run repeatedly for about budget_s seconds."""
+    done = 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < budget_s or done == 0:
+        fn()
+        done += 1
+    return done, time.perf_counter() - t0
+
+
+def bench_output_projection(args, dev, flush, peaks, peaks_src, batch):
+    """y = o (B_v W_o): the fused-weight GEMV of the Llama-2-7B layer (32 heads, r_v 256, d 4096;
+    a 64 MB fp16 weight), o as the decode kernel writes it."""
+    import numpy as np
+    import torch
+    from oracle import palu_oracle as O
+    from rank_kv_cache_gb300 import palu as P
+    from synthetic import gen
+    cfg = gen.ROPE_FP16
+    n, r_v, d = cfg.n_heads, cfg.rank, cfg.hidden
+    fac, _ = gen.factors(cfg)
+    wo = torch.randn((n * cfg.head_dim, d), generator=torch.Generator().manual_seed(7)) / math.sqrt(d)
+    proj = P.OutputProjection(gen.storage_round(fac["v"][1], "f16").to(dev), wo.half().to(dev), n_heads=n,
+                              head_dim=cfg.head_dim, group_size=cfg.group_size, rank_v=r_v, max_batch=batch)
+    o = torch.randn((batch, n * r_v), generator=torch.Generator().manual_seed(8)).to(dev)
+    y = torch.empty((batch, d), dtype=torch.float32, device=dev)
+    for _ in range(10):
+        proj(o, y)
+    torch.cuda.synchronize()
+    ms = event_times(lambda: proj(o, y), 500, flush)
+    nbytes = proj.w.numel() * 2 + o.numel() * 4 + y.numel() * 4
+    med = pct(ms, 50)
+    e = {"batch": batch, "k_dim": n * r_v, "d_model": d, "w_dtype": "f16", "kernel": "oproj_kernel",
+         "gpu_launches_per_step": 1, "kernel_us": stats_us(ms), "bytes": nbytes,
+         "roofline": hbm_roofline(nbytes, med, peaks, peaks_src)}
+    w64 = proj.w.cpu().double().numpy()
+    o64 = o.cpu().double().numpy().reshape(batch, n, r_v)
+    ref = O.project_fused(o64, w64)
+    e["parity_sample"] = {"max_err_over_max_ref": float(np.abs(y.cpu().double().numpy() - ref).max() /
+                                                        np.abs(ref).max())}
+    if not args.no_cpu_baseline:
+        calls, sec = oracle_seconds(lambda: O.project_fused(o64, w64), 2.0)
+        e["cpu_baseline"] = {"value": round(nbytes * calls / sec / 1e9, 4), "unit": "GB/s", "cores": _blas_threads(),
+                             "kind": "oracle", "seconds": round(sec, 2),
+                             "sample": f"{calls} full projections (float64 NumPy, per-head matvecs)"}
+    del proj
+    return e
+
+
+def run_next_rows(args, dev, flush, peaks, peaks_src):
+    """The steps next to the decode kernel, each timed with CUDA events (L2 flushed before each
+    launch) against its own roofline."""
+    import torch
+    out = {}
+    for b in (1, 4):
+        name = f"llama2-7b-oproj-fp16-b{b}"
+        out[name] = bench_output_projection(args, dev, flush, peaks, peaks_src, b)
+        print(f"[bench] {name}: median {out[name]['kernel_us']['median']} us, frac {out[name]['roofline']['frac']}",
+              file=sys.stderr, flush=True)
         torch.cuda.empty_cache()
     return out
 
