@@ -228,6 +228,25 @@ def hadamard(r: int) -> np.ndarray:
 
 
 # ---------------------------------------------------------------------------
+# Latent production (the step before decode)
+# ---------------------------------------------------------------------------
+
+def project_latents(x, a) -> np.ndarray:
+    """H[b, t, g, :] = x[b, t, :] A_g, the latents a new token leaves in the cache ([Palu]
+    "方法细节", SVD rewrite: the layer caches h = x A instead of the key or value itself, and
+    the G-LRD paragraph gives one A_g per group). x [B][T][d], a [n_g][d][r] -> [B][T][n_g][r]."""
+    x = np.asarray(x, np.float64)
+    a = np.asarray(a, np.float64)
+    B, T, _ = x.shape
+    n_g, _, r = a.shape
+    h = np.empty((B, T, n_g, r))
+    for b in range(B):
+        for g in range(n_g):
+            h[b, :, g, :] = x[b] @ a[g]
+    return h
+
+
+# ---------------------------------------------------------------------------
 # int4 per-token latent quantisation
 # ---------------------------------------------------------------------------
 

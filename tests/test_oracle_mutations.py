@@ -113,6 +113,13 @@ def _project_rows_of_next_head(o, w_fused):
     return y
 
 
+def _project_latents_first_group(x, a):
+    # every group's latents taken with group 0's down-projection
+    x, a = np.asarray(x, np.float64), np.asarray(a, np.float64)
+    h = np.einsum("btd,dr->btr", x, a[0])
+    return np.repeat(h[:, :, None, :], a.shape[0], axis=2)
+
+
 ALL_PINS = [getattr(P, n) for n in dir(P) if n.startswith("test_")]
 
 MUTATIONS = {
@@ -128,6 +135,7 @@ MUTATIONS = {
     "softmax_unnormalised": ("softmax_attend", _softmax_no_norm),
     "fuse_wrong_head_block": ("fuse_value_output", _fuse_wrong_head_block),
     "project_rows_of_next_head": ("project_fused", _project_rows_of_next_head),
+    "latents_first_group_only": ("project_latents", _project_latents_first_group),
 }
 
 

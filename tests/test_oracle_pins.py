@@ -407,3 +407,31 @@ def test_int4_huge_and_zero_rows():
     codes, scale = O.quantize_int4(h)
     assert scale[0] == 0 and np.all(codes[0] == 0)
     assert scale[1] == np.float16(65504.0) and np.all(codes[1] == 7)
+
+
+def test_projected_latents_brute_force_tiny():
+    # scalar loops with exact summation: h[b, t, g, m] = sum_e x[b, t, e] A_g[e, m]
+    rng = np.random.default_rng(31)
+    B, T, d, n_g, r = 2, 3, 5, 2, 4
+    x = rng.standard_normal((B, T, d))
+    a = rng.standard_normal((n_g, d, r))
+    h = O.project_latents(x, a)
+    assert h.shape == (B, T, n_g, r)
+    for b in range(B):
+        for t in range(T):
+            for g in range(n_g):
+                for m in range(r):
+                    want = math.fsum(x[b, t, e] * a[g, e, m] for e in range(d))
+                    assert abs(h[b, t, g, m] - want) < 1e-12
+
+
+def test_projected_latents_rebuild_the_keys_at_full_rank():
+    # the SVD rewrite: (x A_g) B_g = x W_g when the factors are exact (full rank r = s*d_h), so
+    # each group's latents rebuild exactly that group's block of keys x W
+    B, T, d, n, s, d_h = 2, 6, 16, 4, 2, 4
+    x, wk, _, _ = _mha_setup(32, B, T, d, n, s, d_h)
+    n_g, r = n // s, s * d_h
+    Ak, Bk = _group_factors(wk, n_g, s, d_h, r)
+    h = O.project_latents(x, Ak)
+    for g in range(n_g):
+        np.testing.assert_allclose(h[:, :, g, :] @ Bk[g], x @ wk[:, g * s * d_h:(g + 1) * s * d_h], atol=1e-11)
