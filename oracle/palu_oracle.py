@@ -177,6 +177,66 @@ def decode(q, hk, hv, bk, seq_lens, group_size: int, *, mode: str = "rope", thet
     return o, lse
 
 
+def decode_hybrid(q, hk, hv, bk, seq_lens, group_size: int, dense_k, dense_v, n_dense, *, mode: str = "rope",
+                  theta: float = 10000.0, positions=None, q_pos=None, heads=None):
+    """Decode over a hybrid cache: a dense segment (the attention-sink tokens and the recent window)
+    next to the G-LRD latent middle ([Puzzle] section 3: the sink page and the local window stay
+    dense, the other completed pages are factorised, and each query attends over dense and
+    factorised pages at once, their partial results merged by online softmax; [Shard] section 7:
+    four fp16 sink tokens and a 64-token fp16 window around the compressed middle).
+
+    Readings: the dense keys are a standard KV cache, i.e. already rotated at their own positions
+    on the RoPE path (unrotated on the absorbed path), so they are scored against q rotated at
+    q_pos; the latent middle is scored as in decode(), at `positions`; one softmax spans both
+    segments. The middle's output stays in latent space (B_v is fused into W_o) while the dense
+    tokens' output is in value space, so head i's attention output is o_lat B_v^(i) + o_dense.
+
+    dense_k, dense_v [B][D][n][d_h]; n_dense [B] (dense tokens used per row). Returns
+    (o_lat [B][n][r_v], o_dense [B][n][d_h], lse [B][n]); rows not in ``heads`` are NaN.
+    """
+    B, n, d_h = q.shape
+    r_v = hv.shape[-1]
+    o_lat = np.full((B, n, r_v), np.nan)
+    o_den = np.full((B, n, d_h), np.nan)
+    lse = np.full((B, n), np.nan)
+    todo = heads if heads is not None else [(b, i) for b in range(B) for i in range(n)]
+    for b, i in todo:
+        T = int(seq_lens[b])
+        D = int(n_dense[b])
+        g, j = _group_of(i, group_size)
+        hk_bg = np.asarray(hk[b, :T, g, :], np.float64)
+        hv_bg = np.asarray(hv[b, :T, g, :], np.float64)
+        kd = np.asarray(dense_k[b, :D, i, :], np.float64)
+        vd = np.asarray(dense_v[b, :D, i, :], np.float64)
+        qi = np.asarray(q[b, i], np.float64)
+        if mode == "rope":
+            if q_pos is None:
+                raise ValueError("the hybrid RoPE path needs q_pos")
+            K = hk_bg @ np.asarray(bk[g], np.float64)[:, j * d_h:(j + 1) * d_h]
+            K_rot = rope_rotate(K, _positions(positions, b, T), theta)
+            q_use = rope_rotate(qi, float(q_pos[b]), theta)
+            s_mid = (K_rot @ q_use) / math.sqrt(d_h) if T else np.zeros(0)
+        elif mode == "absorbed":
+            q_use = qi
+            q_lat = np.asarray(bk[g], np.float64)[:, j * d_h:(j + 1) * d_h] @ qi
+            s_mid = (hk_bg @ q_lat) / math.sqrt(d_h) if T else np.zeros(0)
+        else:
+            raise ValueError(mode)
+        s_den = (kd @ q_use) / math.sqrt(d_h) if D else np.zeros(0)
+        s_all = np.concatenate([s_mid, s_den])
+        if s_all.size == 0:
+            o_lat[b, i], o_den[b, i], lse[b, i] = 0.0, 0.0, -math.inf
+            continue
+        m = s_all.max()
+        e = np.exp(s_all - m)
+        l = e.sum()
+        p = e / l
+        o_lat[b, i] = p[:T] @ hv_bg if T else 0.0
+        o_den[b, i] = p[T:] @ vd if D else 0.0
+        lse[b, i] = m + math.log(l)
+    return o_lat, o_den, lse
+
+
 # ---------------------------------------------------------------------------
 # Uncompressed multi-head attention (the definition the latent path must equal)
 # ---------------------------------------------------------------------------

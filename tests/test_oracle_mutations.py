@@ -120,6 +120,25 @@ def _project_latents_first_group(x, a):
     return np.repeat(h[:, :, None, :], a.shape[0], axis=2)
 
 
+def _decode_hybrid_separate_softmax(q, hk, hv, bk, seq_lens, group_size, dense_k, dense_v, n_dense, **kw):
+    # each segment normalised on its own: the merge of the two partial softmaxes is left out
+    o_lat, lse_mid = O.decode(q, hk, hv, bk, seq_lens, group_size, mode=kw.get("mode", "rope"),
+                              theta=kw.get("theta", 10000.0), positions=kw.get("positions"), q_pos=kw.get("q_pos"))
+    B, n, d_h = q.shape
+    o_den = np.zeros((B, n, d_h))
+    lse = np.array(lse_mid)
+    for b in range(B):
+        D = int(n_dense[b])
+        for i in range(n):
+            qi = np.asarray(q[b, i], np.float64)
+            if kw.get("mode", "rope") == "rope":
+                qi = O.rope_rotate(qi, float(kw["q_pos"][b]), kw.get("theta", 10000.0))
+            if D:
+                sc = np.asarray(dense_k[b, :D, i], np.float64) @ qi / math.sqrt(d_h)
+                o_den[b, i], _ = O.softmax_attend(sc, np.asarray(dense_v[b, :D, i], np.float64))
+    return o_lat, o_den, lse
+
+
 ALL_PINS = [getattr(P, n) for n in dir(P) if n.startswith("test_")]
 
 MUTATIONS = {
@@ -136,6 +155,7 @@ MUTATIONS = {
     "fuse_wrong_head_block": ("fuse_value_output", _fuse_wrong_head_block),
     "project_rows_of_next_head": ("project_fused", _project_rows_of_next_head),
     "latents_first_group_only": ("project_latents", _project_latents_first_group),
+    "hybrid_segments_normalised_apart": ("decode_hybrid", _decode_hybrid_separate_softmax),
 }
 
 

@@ -435,3 +435,80 @@ def test_projected_latents_rebuild_the_keys_at_full_rank():
     h = O.project_latents(x, Ak)
     for g in range(n_g):
         np.testing.assert_allclose(h[:, :, g, :] @ Bk[g], x @ wk[:, g * s * d_h:(g + 1) * s * d_h], atol=1e-11)
+
+
+# ---------------------------------------------------------------------------
+# Hybrid cache: dense sink + window next to the latent middle
+# ---------------------------------------------------------------------------
+
+def _hybrid_split(x, wk, wv, Ak, Av, n, d_h, T, S, W, rope, theta=10000.0):
+    """Tokens [0, S) and [T - W, T) as a dense cache (keys rotated at their positions when rope),
+    tokens [S, T - W) as latents at positions S .. T - W - 1."""
+    B = x.shape[0]
+    dense_idx = list(range(S)) + list(range(T - W, T))
+    D = len(dense_idx)
+    dk = np.zeros((B, D, n, d_h))
+    dv = np.zeros((B, D, n, d_h))
+    for b in range(B):
+        for i in range(n):
+            K = x[b, dense_idx] @ wk[:, i * d_h:(i + 1) * d_h]
+            if rope:
+                K = O.rope_rotate(K, np.array(dense_idx, np.float64), theta)
+            dk[b, :, i] = K
+            dv[b, :, i] = x[b, dense_idx] @ wv[:, i * d_h:(i + 1) * d_h]
+    mid = x[:, S:T - W]
+    hk = np.einsum("btd,gdr->btgr", mid, Ak)
+    hv = np.einsum("btd,gdr->btgr", mid, Av)
+    pos = np.tile(np.arange(S, T - W), (B, 1))
+    return dk, dv, hk, hv, pos
+
+
+@pytest.mark.parametrize("mode", ["rope", "absorbed"])
+def test_hybrid_at_full_rank_equals_uncompressed_mha_over_all_tokens(mode):
+    # exact factors: sink + latent middle + window must be plain attention over every token
+    B, T, d, n, s, d_h = 2, 14, 32, 4, 2, 4
+    x, wk, wv, q = _mha_setup(41, B, T, d, n, s, d_h)
+    n_g, r = n // s, s * d_h
+    Ak, Bk = _group_factors(wk, n_g, s, d_h, r)
+    Av, Bv = _group_factors(wv, n_g, s, d_h, r)
+    S, W = 2, 3
+    dk, dv, hk, hv, pos = _hybrid_split(x, wk, wv, Ak, Av, n, d_h, T, S, W, mode == "rope")
+    qp = [T - 1] * B
+    o_lat, o_den, lse = O.decode_hybrid(q, hk, hv, Bk, [T - S - W] * B, s, dk, dv, [S + W] * B, mode=mode,
+                                        positions=pos, q_pos=qp)
+    a, lse_ref = O.mha_decode(q, x, wk, wv, [T] * B, rope=(mode == "rope"), q_pos=qp)
+    for b in range(B):
+        for i in range(n):
+            g, j = i // s, i % s
+            np.testing.assert_allclose(o_lat[b, i] @ Bv[g][:, j * d_h:(j + 1) * d_h] + o_den[b, i], a[b, i],
+                                       atol=1e-11)
+    np.testing.assert_allclose(lse, lse_ref, atol=1e-11)
+
+
+@pytest.mark.parametrize("mode", ["rope", "absorbed"])
+def test_hybrid_without_dense_tokens_is_the_latent_decode(mode):
+    q, hk, hv, bk = _tiny(seed=42, B=2, T=7, n=4, s=2, d_h=4, r=4, r_v=3)
+    dk = np.zeros((2, 0, 4, 4))
+    qp = [6, 6]
+    o_lat, o_den, lse = O.decode_hybrid(q, hk, hv, bk, [7, 5], 2, dk, dk, [0, 0], mode=mode, q_pos=qp)
+    o, lse_ref = O.decode(q, hk, hv, bk, [7, 5], 2, mode=mode, q_pos=qp)
+    np.testing.assert_allclose(o_lat, o, atol=1e-13)
+    np.testing.assert_allclose(lse, lse_ref, atol=1e-13)
+    assert np.all(o_den == 0)
+
+
+def test_hybrid_with_an_empty_middle_is_dense_softmax_attention():
+    import scipy.special
+    rng = np.random.default_rng(43)
+    B, n, d_h, D = 1, 2, 4, 5
+    q = rng.standard_normal((B, n, d_h))
+    dk = rng.standard_normal((B, D, n, d_h))
+    dv = rng.standard_normal((B, D, n, d_h))
+    hk = np.zeros((B, 1, 1, 3))
+    bk = np.zeros((1, 3, 2 * d_h))
+    o_lat, o_den, lse = O.decode_hybrid(q, hk, hk, bk, [0], 2, dk, dv, [D], mode="rope", q_pos=[0])
+    for i in range(n):
+        sc = dk[0, :, i] @ q[0, i] / math.sqrt(d_h)   # q_pos 0: the query is not rotated
+        np.testing.assert_allclose(o_den[0, i], scipy.special.softmax(sc) @ dv[0, :, i], atol=1e-13)
+        assert abs(lse[0, i] - scipy.special.logsumexp(sc)) < 1e-13
+    assert np.all(o_lat == 0)
