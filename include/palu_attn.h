@@ -279,6 +279,73 @@ palu_status_t palu_output_proj(const void* W_fused, palu_dtype_t w_dtype, int64_
                                const float* o, int batch, float* y, void* workspace, size_t workspace_bytes,
                                palu_stream_t stream);
 
+/*
+ * Decode over a hybrid cache: dense attention-sink and recent-window tokens kept as a standard
+ * KV cache next to the G-LRD latent middle ("PuzzleKV" section 3: the sink page and the local
+ * window stay dense, the other pages are factorised, and each query attends over both kinds of
+ * page, the partial results merged by online softmax; "Shard" section 7: four fp16 sink tokens
+ * and a 64-token fp16 window around the compressed middle).
+ *
+ *   dense->k, dense->v  device [max_rows][capacity][n_heads][head_dim] in dense->dtype (F32, F16
+ *                       or BF16). On the RoPE path the keys are stored rotated at their own
+ *                       positions (as a dense KV cache holds them); on the absorbed path unrotated.
+ *   dense->n_tokens     device [batch] int32: tokens 0 .. n_tokens[b] - 1 of row b are attended
+ *                       (their order does not matter); a count outside [0, capacity] is clamped
+ *                       and recorded in the error word.
+ *
+ * The other arguments are palu_decode_attn's, for the latent middle only: seq_lens counts its
+ * tokens and `positions` gives their positions (the middle usually starts after the sink tokens,
+ * so the default t is rarely right). q_pos is required on the RoPE path (the position of the
+ * decoded token). lse is required. One softmax spans both segments; the outputs are
+ *   out       [batch][n_heads][rank_v]    sum over the middle of p h_v (latent space)
+ *   out_dense [batch][n_heads][head_dim]  sum over the dense tokens of p v (value space)
+ *   lse       [batch][n_heads]            natural log-sum-exp over all tokens
+ * so head i's attention output is out_i B_v^(i) + out_dense_i (out feeds palu_output_proj with
+ * the fused weight, out_dense the plain W_o). Supported head_dim: 32, 64, 96 or 128 (else
+ * PALU_ERR_UNSUPPORTED). Two launches on `stream`: the latent decode, then the dense merge.
+ */
+typedef struct palu_dense_cache {
+  const void* k;
+  const void* v;
+  const int32_t* n_tokens;
+  int64_t capacity;
+  palu_dtype_t dtype;
+} palu_dense_cache;
+
+palu_status_t palu_decode_hybrid(palu_attn_t h, const void* q, const palu_cache* cache, const int32_t* seq_lens,
+                                 const int32_t* positions, const int32_t* q_pos, int batch, int64_t max_seq_len,
+                                 const palu_dense_cache* dense, float* out, float* out_dense, float* lse,
+                                 palu_stream_t stream);
+
+/*
+ * Latent production: the step that fills the cache ("方法细节", SVD-rewrite paragraph: the
+ * layer caches h = x A in place of k = x W and v = x W_v; G-LRD paragraph: one A_g per group;
+ * "补充细节": per-token quantisation of the cached latents). For n_new new tokens of each
+ * batch row, H_k = x A_k,g and H_v = x A_v,g are computed on the tensor cores (fp16 or bf16
+ * operands, fp32 accumulation) and written into the cache at tokens dst_slot[b] ..
+ * dst_slot[b] + n_new - 1 of row b, in the cache's dtype: F32 values as accumulated, F16/BF16
+ * rounded to nearest, INT4 quantised per token and group exactly as palu_append_latents does
+ * (the same codes and scales for the same fp32 values).
+ *
+ * palu_down_proj_size / palu_prepare_down_proj (once per layer, an offline transform): A_k and
+ * A_v are device arrays [n_g][d_model][rank] in a_dtype (F32, F16, BF16), the Hadamard-folded
+ * factors where the latents are rotated. W (device, 16-byte aligned, palu_down_proj_size
+ * bytes) receives [2][n_g][rank][d_model] in w_dtype (F16 or BF16): each A_g transposed.
+ *
+ * palu_project_latents (per prefill or decode step): x device [batch][n_new][d_model] in
+ * w_dtype, 16-byte aligned; W as prepared; cache and dst_slot as for palu_append_latents.
+ * Supported: rank_k = rank_v in {128, 256}, key and value caches of one dtype, d_model a
+ * multiple of 64, batch * n_new < 2^31 (else PALU_ERR_UNSUPPORTED). A slot past the capacity
+ * is recorded in the error word and that token's rows are skipped. Asynchronous on `stream`.
+ */
+palu_status_t palu_down_proj_size(palu_attn_t h, int64_t d_model, size_t* bytes);
+palu_status_t palu_prepare_down_proj(palu_attn_t h, const void* A_k, const void* A_v, palu_dtype_t a_dtype,
+                                     int64_t d_model, palu_dtype_t w_dtype, void* W, size_t W_bytes,
+                                     palu_stream_t stream);
+palu_status_t palu_project_latents(palu_attn_t h, const void* W, palu_dtype_t w_dtype, int64_t d_model,
+                                   const void* x, const palu_cache* cache, const int32_t* dst_slot, int batch,
+                                   int n_new, palu_stream_t stream);
+
 /* Free the host handle. Does not synchronise: no work on it may be in flight. NULL is fine. */
 palu_status_t palu_destroy(palu_attn_t h);
 

@@ -889,6 +889,13 @@ bool encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, 
 
 }  // namespace
 
+bool tma_available() { return encode_fn() != nullptr; }
+
+bool tma_encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const cuuint64_t* dims,
+                const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle sw) {
+  return encode_fn() != nullptr && encode(m, dt, rank, base, dims, strides, box, sw);
+}
+
 bool tc_supported(const DecodeArgs& a) {
   const bool i4 = a.k_dtype == kINT4;
   return (a.k_dtype == kF16 || a.k_dtype == kBF16 || i4) && a.v_dtype == a.k_dtype &&

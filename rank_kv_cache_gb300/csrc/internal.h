@@ -1,6 +1,7 @@
 // Internal interface between the C ABI (palu_host.cu) and the kernel translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -84,6 +85,52 @@ cudaError_t launch_debug_int4_operand(const void* hk, const __half* k_scale, int
                                       int64_t n_tokens, uint16_t* codes, float* deq, ErrWord* err, cudaStream_t st);
 cudaError_t launch_debug_int4_dp2a(const void* cache, int64_t capacity, int n_g, int batch, int64_t n_tokens,
                                    const int32_t* weights, int32_t* sums, cudaStream_t st);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (decode_tc.cu); false when the
+// driver offers no entry point or rejects the map
+bool tma_available();
+bool tma_encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const cuuint64_t* dims,
+                const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle sw);
+
+// latent production H = x A on tcgen05 (prefill.cu)
+struct ProjectArgs {
+  void* cache[2];             // key and value latent caches
+  __half* scale[2];           // int4 scales (nullable otherwise)
+  int cache_dtype;
+  int64_t capacity;
+  int n_g, rank;
+  int64_t d;                  // d_model
+  const int32_t* dst_slot;    // [batch]
+  int n_new;
+  int64_t M;                  // batch * n_new rows of x
+  ErrWord* err;
+  uint64_t wait_ns;
+};
+cudaError_t launch_project_latents(const void* x, const void* w, int bf16, const ProjectArgs& a, cudaStream_t st);
+cudaError_t launch_prepare_down_proj(const void* a_k, const void* a_v, int a_dtype, int n_g, int rank, int64_t d,
+                                     int w_dtype, void* w, cudaStream_t st);
+
+// hybrid cache: the dense segment merged with the latent middle's decode (hybrid.cu)
+struct DenseArgs {
+  const void* k;              // [rows][capacity][n_heads][dh] dense keys (rotated at their positions on the RoPE path)
+  const void* v;              // same layout, values
+  int dtype;                  // kF32, kF16 or kBF16
+  const int32_t* n_tokens;    // [batch] dense tokens per row
+  int64_t capacity;
+  int n_heads, dh, rv, batch;
+  int rope;                   // rotate the query at q_pos
+  const int32_t* q_pos;
+  const float2* rope_tab;     // [max_pos][dh/2]
+  int64_t max_pos;
+  const void* q;
+  int q_dtype;
+  float qscale;               // log2(e) / sqrt(dh)
+  float* out;                 // [batch][n_heads][rv]: the middle's output, rescaled in place
+  float* out_dense;           // [batch][n_heads][dh]
+  float* lse;                 // [batch][n_heads]: the middle's lse in, the merged lse out
+  ErrWord* err;
+};
+cudaError_t launch_merge_dense(const DenseArgs& d, cudaStream_t st);
 
 // TMA-streaming absorbed-mode kernel (decode_abs.cu)
 bool abs_supported(const DecodeArgs& a);

@@ -313,6 +313,74 @@ palu_status_t palu_append_latents(palu_attn_t h, const palu_cache* cache, const 
   return e == cudaSuccess ? PALU_OK : PALU_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------------------- latent production
+// The prepared down-projection operand is [2][n_g][rank][d_model] (A_k then A_v, each A_g
+// transposed); the tensor-core kernel takes rank 128 or 256 and d_model in multiples of 64.
+static palu_status_t check_down_proj(const palu_attn* h, int64_t d_model) {
+  if (!h || d_model <= 0) return PALU_ERR_INVALID_ARG;
+  if (h->d.rank_k != h->d.rank_v || (h->d.rank_k != 128 && h->d.rank_k != 256) || d_model % 64 ||
+      d_model > (int64_t(1) << 31))
+    return PALU_ERR_UNSUPPORTED;
+  return PALU_OK;
+}
+
+palu_status_t palu_down_proj_size(palu_attn_t h, int64_t d_model, size_t* bytes) {
+  if (!bytes) return PALU_ERR_INVALID_ARG;
+  const palu_status_t st = check_down_proj(h, d_model);
+  if (st != PALU_OK) return st;
+  *bytes = (size_t)2 * h->n_g * h->d.rank_k * d_model * 2;
+  return PALU_OK;
+}
+
+palu_status_t palu_prepare_down_proj(palu_attn_t h, const void* A_k, const void* A_v, palu_dtype_t a_dtype,
+                                     int64_t d_model, palu_dtype_t w_dtype, void* W, size_t W_bytes,
+                                     palu_stream_t stream) {
+  palu_status_t st = check_down_proj(h, d_model);
+  if (st != PALU_OK) return st;
+  if ((unsigned)a_dtype > PALU_BF16 || (w_dtype != PALU_F16 && w_dtype != PALU_BF16)) return PALU_ERR_INVALID_ARG;
+  const size_t ie = a_dtype == PALU_F32 ? 4 : 2;
+  if (!A_k || !A_v || !W || (uintptr_t)A_k % ie || (uintptr_t)A_v % ie || (uintptr_t)W % 16) return PALU_ERR_INVALID_ARG;
+  if (W_bytes < (size_t)2 * h->n_g * h->d.rank_k * d_model * 2) return PALU_ERR_INVALID_ARG;
+  if (cudaSetDevice(h->device) != cudaSuccess) return PALU_ERR_CUDA;
+  const cudaError_t e = launch_prepare_down_proj(A_k, A_v, to_dt(a_dtype), h->n_g, h->d.rank_k, d_model,
+                                                 to_dt(w_dtype), W, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PALU_OK : PALU_ERR_CUDA;
+}
+
+palu_status_t palu_project_latents(palu_attn_t h, const void* W, palu_dtype_t w_dtype, int64_t d_model,
+                                   const void* x, const palu_cache* cache, const int32_t* dst_slot, int batch,
+                                   int n_new, palu_stream_t stream) {
+  palu_status_t st = check_down_proj(h, d_model);
+  if (st != PALU_OK) return st;
+  st = check_cache(h, cache);
+  if (st != PALU_OK) return st;
+  if (h->d.k_dtype != h->d.v_dtype) return PALU_ERR_UNSUPPORTED;
+  if (w_dtype != PALU_F16 && w_dtype != PALU_BF16) return PALU_ERR_INVALID_ARG;
+  if (batch < 0 || batch > h->d.max_batch || n_new < 0) return PALU_ERR_INVALID_ARG;
+  if ((int64_t)batch * n_new >= (int64_t(1) << 31)) return PALU_ERR_UNSUPPORTED;
+  if (batch == 0 || n_new == 0) return PALU_OK;
+  if (!W || !x || !dst_slot || (uintptr_t)W % 16 || (uintptr_t)x % 16) return PALU_ERR_INVALID_ARG;
+  if (cudaSetDevice(h->device) != cudaSuccess) return PALU_ERR_CUDA;
+  ProjectArgs a{};
+  a.cache[0] = cache->hk;
+  a.cache[1] = cache->hv;
+  a.scale[0] = static_cast<__half*>(cache->k_scale);
+  a.scale[1] = static_cast<__half*>(cache->v_scale);
+  a.cache_dtype = to_dt(h->d.k_dtype);
+  a.capacity = cache->capacity;
+  a.n_g = h->n_g;
+  a.rank = h->d.rank_k;
+  a.d = d_model;
+  a.dst_slot = dst_slot;
+  a.n_new = n_new;
+  a.M = (int64_t)batch * n_new;
+  a.err = reinterpret_cast<ErrWord*>(h->ws + h->L.err);
+  a.wait_ns = 1000000000ull;
+  const cudaError_t e = launch_project_latents(x, W, w_dtype == PALU_BF16, a, reinterpret_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return PALU_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? PALU_OK : PALU_ERR_CUDA;
+}
+
 // Shape, type and workspace fields of a decode launch (the per-call pointers are set by the caller).
 static void fill_args(const palu_attn* h, const palu_cache* cache, int batch, int64_t max_seq_len, DecodeArgs& a) {
   const palu_attn_desc& d = h->d;
@@ -419,6 +487,51 @@ palu_status_t palu_decode_attn(palu_attn_t h, const void* q, const palu_cache* c
   if (e == cudaSuccess)
     e = use_tc ? launch_decode_tc(a, s) : use_abs ? launch_decode_abs(a, s) : launch_decode_simt(mode, a, s);
   if (tr && e == cudaSuccess) e = cudaEventRecord(tr[1], s);
+  return e == cudaSuccess ? PALU_OK : PALU_ERR_CUDA;
+}
+
+palu_status_t palu_decode_hybrid(palu_attn_t h, const void* q, const palu_cache* cache, const int32_t* seq_lens,
+                                 const int32_t* positions, const int32_t* q_pos, int batch, int64_t max_seq_len,
+                                 const palu_dense_cache* dense, float* out, float* out_dense, float* lse,
+                                 palu_stream_t stream) {
+  if (!h || !dense) return PALU_ERR_INVALID_ARG;
+  if (h->d.head_dim > 128 || h->d.head_dim % 32) return PALU_ERR_UNSUPPORTED;
+  if (batch < 0 || batch > h->d.max_batch) return PALU_ERR_INVALID_ARG;
+  if (batch == 0) return PALU_OK;
+  if (!lse || !out_dense || (uintptr_t)out_dense % 4 || (uintptr_t)lse % 4) return PALU_ERR_INVALID_ARG;
+  if (h->d.mode == PALU_MODE_ROPE && !q_pos) return PALU_ERR_INVALID_ARG;
+  if (!dense->k || !dense->v || !dense->n_tokens || dense->capacity <= 0 || dense->capacity > (int64_t(1) << 31) ||
+      (unsigned)dense->dtype > PALU_BF16)
+    return PALU_ERR_INVALID_ARG;
+  const size_t es = dense->dtype == PALU_F32 ? 4 : 2;
+  if ((uintptr_t)dense->k % es || (uintptr_t)dense->v % es) return PALU_ERR_INVALID_ARG;
+  // the latent middle: out and lse hold its own softmax until the merge below
+  palu_status_t st = palu_decode_attn(h, q, cache, seq_lens, positions, q_pos, batch, max_seq_len, out, lse, stream);
+  if (st != PALU_OK) return st;
+  DecodeArgs a{};
+  fill_args(h, cache, batch, max_seq_len, a);
+  DenseArgs d{};
+  d.k = dense->k;
+  d.v = dense->v;
+  d.dtype = to_dt(dense->dtype);
+  d.n_tokens = dense->n_tokens;
+  d.capacity = dense->capacity;
+  d.n_heads = h->d.n_heads;
+  d.dh = h->d.head_dim;
+  d.rv = h->d.rank_v;
+  d.batch = batch;
+  d.rope = h->d.mode == PALU_MODE_ROPE;
+  d.q_pos = q_pos;
+  d.rope_tab = a.rope;
+  d.max_pos = a.max_pos;
+  d.q = q;
+  d.q_dtype = a.q_dtype;
+  d.qscale = a.qscale;
+  d.out = out;
+  d.out_dense = out_dense;
+  d.lse = lse;
+  d.err = a.err;
+  const cudaError_t e = launch_merge_dense(d, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PALU_OK : PALU_ERR_CUDA;
 }
 

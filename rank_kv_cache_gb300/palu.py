@@ -33,7 +33,8 @@ EXPORTS = ("palu_attn_workspace_size", "palu_attn_create", "palu_append_latents"
            "palu_destroy", "palu_attn_check", "palu_status_string", "palu_debug_dequant",
            "palu_attn_trace_enable", "palu_attn_trace_read", "palu_decode_attn_noalloc", "palu_decode_plan",
            "palu_debug_int4_operand", "palu_debug_int4_dp2a", "palu_attn_trace_times",
-           "palu_fuse_value_output", "palu_output_proj_workspace_size", "palu_output_proj")
+           "palu_fuse_value_output", "palu_output_proj_workspace_size", "palu_output_proj",
+           "palu_down_proj_size", "palu_prepare_down_proj", "palu_project_latents", "palu_decode_hybrid")
 PALU_TRACE_CAPACITY = 4096
 
 
@@ -49,6 +50,11 @@ class palu_attn_desc(ctypes.Structure):
 class palu_cache(ctypes.Structure):
     _fields_ = [("hk", ctypes.c_void_p), ("hv", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
                 ("v_scale", ctypes.c_void_p), ("capacity", ctypes.c_int64)]
+
+
+class palu_dense_cache(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("n_tokens", ctypes.c_void_p),
+                ("capacity", ctypes.c_int64), ("dtype", ctypes.c_int)]
 
 
 class PaluError(RuntimeError):
@@ -82,6 +88,11 @@ def _load():
         "palu_output_proj": (I, [P, I, I64, I64, P, I, P, P, SZ, P]),
         "palu_debug_int4_operand": (I, [P, ctypes.POINTER(palu_cache), I, I64, P, P, P]),
         "palu_debug_int4_dp2a": (I, [P, ctypes.POINTER(palu_cache), I, I, I64, P, P, P]),
+        "palu_down_proj_size": (I, [P, I64, ctypes.POINTER(SZ)]),
+        "palu_prepare_down_proj": (I, [P, P, P, I, I64, I, P, SZ, P]),
+        "palu_project_latents": (I, [P, P, I, I64, P, ctypes.POINTER(palu_cache), P, I, I, P]),
+        "palu_decode_hybrid": (I, [P, P, ctypes.POINTER(palu_cache), P, P, P, I, I64,
+                                   ctypes.POINTER(palu_dense_cache), P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -194,6 +205,29 @@ def palu_output_proj_workspace_size(k_dim: int, d_model: int, max_batch: int):
 def palu_output_proj(w_fused: int, w_dtype: int, k_dim: int, d_model: int, o: int, batch: int, y: int,
                      workspace: int, ws_bytes: int, stream: int) -> int:
     return _lib.palu_output_proj(w_fused, w_dtype, k_dim, d_model, o, batch, y, workspace, ws_bytes, stream)
+
+
+def palu_down_proj_size(h, d_model: int):
+    n = ctypes.c_size_t(0)
+    st = _lib.palu_down_proj_size(h, d_model, ctypes.byref(n))
+    return st, n.value
+
+
+def palu_prepare_down_proj(h, a_k: int, a_v: int, a_dtype: int, d_model: int, w_dtype: int, w: int, w_bytes: int,
+                           stream: int) -> int:
+    return _lib.palu_prepare_down_proj(h, a_k, a_v, a_dtype, d_model, w_dtype, w, w_bytes, stream)
+
+
+def palu_project_latents(h, w: int, w_dtype: int, d_model: int, x: int, cache: palu_cache, dst_slot: int,
+                         batch: int, n_new: int, stream: int) -> int:
+    return _lib.palu_project_latents(h, w, w_dtype, d_model, x, ctypes.byref(cache), dst_slot, batch, n_new, stream)
+
+
+def palu_decode_hybrid(h, q: int, cache: palu_cache, seq_lens: int, positions, q_pos, batch: int,
+                       max_seq_len: int, dense: palu_dense_cache, out: int, out_dense: int, lse: int,
+                       stream: int) -> int:
+    return _lib.palu_decode_hybrid(h, q, ctypes.byref(cache), seq_lens, positions, q_pos, batch, max_seq_len,
+                                   ctypes.byref(dense), out, out_dense, lse, stream)
 
 
 def check(status: int, what: str = "palu") -> None:
@@ -313,6 +347,58 @@ class PaluAttention:
                               _ptr(q_pos), B, int(max_seq_len), _ptr(out), _ptr(lse), _stream_handle(stream))
         check(st, "palu_decode_attn")
         return out
+
+    def decode_hybrid(self, q, cache: LatentCache, seq_lens, dense_k, dense_v, dense_n, *, max_seq_len,
+                      positions=None, q_pos=None, out=None, out_dense=None, lse=None, stream=None):
+        """Decode over the latent middle (cache, seq_lens, positions) and a dense segment
+        (dense_k / dense_v [rows][capacity][n_heads][head_dim], dense_n [batch] tokens per row),
+        one softmax over both. Returns (out [B][n][rank_v], out_dense [B][n][head_dim], lse [B][n])."""
+        torch = _torch()
+        _require_contiguous(q=q, seq_lens=seq_lens, positions=positions, q_pos=q_pos, dense_k=dense_k,
+                            dense_v=dense_v, dense_n=dense_n)
+        B = q.shape[0]
+        if out is None:
+            out = torch.empty((B, self.n_heads, self.rank_v), dtype=torch.float32, device=q.device)
+        if out_dense is None:
+            out_dense = torch.empty((B, self.n_heads, self.head_dim), dtype=torch.float32, device=q.device)
+        if lse is None:
+            lse = torch.empty((B, self.n_heads), dtype=torch.float32, device=q.device)
+        ddt = {torch.float32: PALU_F32, torch.float16: PALU_F16, torch.bfloat16: PALU_BF16}[dense_k.dtype]
+        dense = palu_dense_cache(_ptr(dense_k), _ptr(dense_v), _ptr(dense_n), int(dense_k.shape[1]), ddt)
+        st = palu_decode_hybrid(self.handle, _ptr(q), cache.c_struct(), _ptr(seq_lens), _ptr(positions), _ptr(q_pos),
+                                B, int(max_seq_len), dense, _ptr(out), _ptr(out_dense), _ptr(lse),
+                                _stream_handle(stream))
+        check(st, "palu_decode_hybrid")
+        return out, out_dense, lse
+
+    def prepare_down_proj(self, a_k, a_v, *, dtype="f16", stream=None):
+        """The down-projections A_k, A_v ([n_g][d_model][rank] device tensors) as the tensor-core
+        operand for project(): a [2][n_g][rank][d_model] tensor of `dtype` ("f16" or "bf16")."""
+        torch = _torch()
+        _require_contiguous(a_k=a_k, a_v=a_v)
+        if a_k.dtype != a_v.dtype or a_k.shape != a_v.shape:
+            raise ValueError("a_k and a_v must share dtype and shape")
+        d_model = int(a_k.shape[1])
+        st, nbytes = palu_down_proj_size(self.handle, d_model)
+        check(st, "palu_down_proj_size")
+        tdt = {"f16": torch.float16, "bf16": torch.bfloat16}[dtype]
+        w = torch.empty((2, a_k.shape[0], self.rank_k, d_model), dtype=tdt, device=a_k.device)
+        src = {torch.float32: PALU_F32, torch.float16: PALU_F16, torch.bfloat16: PALU_BF16}[a_k.dtype]
+        check(palu_prepare_down_proj(self.handle, _ptr(a_k), _ptr(a_v), src, d_model, DTYPES[dtype], _ptr(w),
+                                     nbytes, _stream_handle(stream)), "palu_prepare_down_proj")
+        return w
+
+    def project(self, w, x, cache: LatentCache, dst_slot, stream=None):
+        """H = x A for x [batch][n_new][d_model] (the dtype of w), written into the cache at
+        dst_slot[b] .. dst_slot[b] + n_new - 1."""
+        torch = _torch()
+        _require_contiguous(w=w, x=x, dst_slot=dst_slot)
+        if x.dtype != w.dtype:
+            raise ValueError("x and w must share a dtype")
+        wdt = {torch.float16: PALU_F16, torch.bfloat16: PALU_BF16}[w.dtype]
+        st = palu_project_latents(self.handle, _ptr(w), wdt, int(w.shape[-1]), _ptr(x), cache.c_struct(),
+                                  _ptr(dst_slot), int(x.shape[0]), int(x.shape[1]), _stream_handle(stream))
+        check(st, "palu_project_latents")
 
     def plan(self, cache_capacity, batch, max_seq_len):
         """(kernel, n_splits, launches) that decode() would use; host-only."""
