@@ -274,7 +274,7 @@ class GpuWorkload:
     """Device-resident workload: the latent cache drawn on the device and filled through the
     append kernel one batch row at a time, plus the per-step inputs."""
 
-    def __init__(self, cfg, device):
+    def __init__(self, cfg, device, max_position=0):
         import torch
         from rank_kv_cache_gb300 import palu as P
         from synthetic import gen
@@ -286,7 +286,7 @@ class GpuWorkload:
         self.attn = P.PaluAttention(self.bk_host.to(device), n_heads=cfg.n_heads, head_dim=cfg.head_dim,
                                     group_size=cfg.group_size, rank_k=r, rank_v=r, latent_dtype=lat,
                                     q_dtype=cfg.q_dtype, mode=cfg.mode, rope_theta=cfg.theta, max_batch=B,
-                                    max_tokens=T)
+                                    max_tokens=T, max_position=max_position)
         self.cache = P.LatentCache(B, T, n_g, r, r, lat, device=device)
         src_dt = "f32" if lat in ("int4", "f32") else lat
         tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[src_dt]
@@ -632,6 +632,120 @@ def bench_output_projection(args, dev, flush, peaks, peaks_src, batch):
     return e
 
 
+def tensor_roofline(flops, ms, peaks, peaks_src):
+    ach = flops / (ms / 1e3) / 1e12
+    tc = float(peaks["bf16_tflops"])
+    return {"bound": "tensor", "achieved": round(ach, 1), "peak": tc, "unit": "TFLOP/s", "frac": round(ach / tc, 4),
+            "roofline_us": round(flops / (tc * 1e12) * 1e6, 2), "peak_source": f"bf16_tflops of {peaks_src}",
+            "duration": "median launch"}
+
+
+def bench_prefill(args, dev, flush, peaks, peaks_src, batch, T, latent_dtype):
+    """H = x A for a prefill of batch x T tokens of the Llama-2-7B layer (d 4096, 8 groups, rank 256,
+    key and value), written into a cache of latent_dtype; x fp16."""
+    import numpy as np
+    import torch
+    from oracle import palu_oracle as O
+    from rank_kv_cache_gb300 import palu as P
+    from synthetic import gen
+    cfg = gen.ROPE_INT4 if latent_dtype == "int4" else gen.ROPE_FP16
+    fac, _ = gen.factors(cfg)
+    bk = gen.storage_round(fac["k"][1], "f16").to(dev)
+    attn = P.PaluAttention(bk, n_heads=cfg.n_heads, head_dim=cfg.head_dim, group_size=cfg.group_size,
+                           rank_k=cfg.rank, rank_v=cfg.rank, latent_dtype=latent_dtype, q_dtype="f16", mode="rope",
+                           max_batch=batch, max_tokens=T)
+    cache = P.LatentCache(batch, T, cfg.n_groups, cfg.rank, cfg.rank, latent_dtype, device=dev)
+    ak = gen.storage_round(fac["k"][0], "f16").to(dev)
+    av = gen.storage_round(fac["v"][0], "f16").to(dev)
+    w = attn.prepare_down_proj(ak, av, dtype="f16")
+    g = torch.Generator(device=dev)
+    g.manual_seed(11)
+    x = torch.randn((batch, T, cfg.hidden), generator=g, device=dev, dtype=torch.float32).half()
+    slot = torch.zeros(batch, dtype=torch.int32, device=dev)
+    for _ in range(5):
+        attn.project(w, x, cache, slot)
+    torch.cuda.synchronize()
+    ms = event_times(lambda: attn.project(w, x, cache, slot), 50, flush)
+    attn.check_device()
+    M, d, N = batch * T, cfg.hidden, 2 * cfg.n_groups * cfg.rank
+    flops = 2 * M * d * N
+    med = pct(ms, 50)
+    e = {"batch": batch, "tokens": T, "d_model": d, "n_out": N, "x_dtype": "f16", "latent_dtype": latent_dtype,
+         "kernel": "project_latents_kernel", "gpu_launches_per_step": 1, "kernel_us": stats_us(ms), "flops": flops,
+         "roofline": tensor_roofline(flops, med, peaks, peaks_src)}
+    # parity sample and oracle baseline: 64 tokens of batch row 0, group 0 of the key side
+    xs = x[0, :64].float().cpu().double().numpy()[None]
+    a0 = ak[:1].float().cpu().double().numpy()
+    ref = O.project_latents(xs, a0)[0, :, 0, :]
+    if latent_dtype == "int4":
+        codes, sc = O.quantize_int4(ref.astype(np.float32))
+        got = O.dequant_int4(cache.hk[0, :64, 0].cpu().numpy(), cache.k_scale[0, :64, 0].cpu().numpy())
+        e["parity_sample"] = {"tokens": 64, "max_abs_err_vs_oracle_dequant": float(np.abs(got - O.dequant_int4(
+            O.pack_int4(codes), sc)).max()), "scale_units_max": float(np.abs(got - ref).max() / float(sc.max()))}
+    else:
+        got = cache.hk[0, :64, 0].float().cpu().double().numpy()
+        e["parity_sample"] = {"tokens": 64, "max_err_over_max_ref": float(np.abs(got - ref).max() / np.abs(ref).max())}
+    if not args.no_cpu_baseline:
+        a_all = ak.float().cpu().double().numpy()
+        calls, sec = oracle_seconds(lambda: O.project_latents(xs, a_all), 2.0)
+        toks = 64 * calls
+        e["cpu_baseline"] = {"value": round(2 * toks * d * (N // 2) / sec / 1e12, 6), "unit": "TFLOP/s",
+                             "cores": _blas_threads(), "kind": "oracle", "seconds": round(sec, 2),
+                             "sample": f"{calls} x 64 tokens of the key side (float64 NumPy)"}
+    attn.close()
+    return e
+
+
+def bench_hybrid(args, dev, flush, peaks, peaks_src, sinks=4, window=64):
+    """Decode over a hybrid cache: the Llama-2-7B int4 layer at batch 4 with `sinks` + `window`
+    dense fp16 tokens around a latent middle of 65536 - sinks - window tokens (positions
+    sinks .. sinks + T_mid - 1, the query at 65535). Times the whole call (latent decode + dense
+    merge) and, from the library's trace, the latent decode kernel alone."""
+    import torch
+    from rank_kv_cache_gb300 import palu as P
+    from synthetic import gen
+    cfg = gen.ROPE_INT4.with_(T=gen.ROPE_INT4.T - sinks - window)
+    wl = GpuWorkload(cfg, dev, max_position=gen.ROPE_INT4.T)
+    B, T, n, d_h = cfg.batch, cfg.T, cfg.n_heads, cfg.head_dim
+    D = sinks + window
+    g = torch.Generator(device=dev)
+    g.manual_seed(13)
+    dk = torch.randn((B, D, n, d_h), generator=g, device=dev).half()
+    dv = torch.randn((B, D, n, d_h), generator=g, device=dev).half()
+    nd = torch.full((B,), D, dtype=torch.int32, device=dev)
+    pos = (torch.arange(T, dtype=torch.int32, device=dev) + sinks).repeat(B, 1).contiguous()
+    qp = torch.full((B,), sinks + T + window - 1, dtype=torch.int32, device=dev)
+    seq = torch.full((B,), T, dtype=torch.int32, device=dev)
+    out = torch.empty((B, n, cfg.rank), dtype=torch.float32, device=dev)
+    od = torch.empty((B, n, d_h), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, n), dtype=torch.float32, device=dev)
+
+    def call():
+        wl.attn.decode_hybrid(wl.q, wl.cache, seq, dk, dv, nd, max_seq_len=T, positions=pos, q_pos=qp, out=out,
+                              out_dense=od, lse=lse)
+
+    for _ in range(5):
+        call()
+    torch.cuda.synchronize()
+    P.check(P.palu_attn_trace_enable(wl.attn.handle, 1))
+    ms = event_times(call, 50, flush)
+    st, kms = P.palu_attn_trace_times(wl.attn.handle)
+    P.check(st)
+    P.check(P.palu_attn_trace_enable(wl.attn.handle, 0))
+    wl.attn.check_device()
+    work = step_work(cfg)
+    dense_bytes = 2 * B * D * n * d_h * 2
+    e = {"batch": B, "sink_tokens": sinks, "window_tokens": window, "latent_tokens": T, "latent_dtype": "int4",
+         "dense_dtype": "f16", "kernels": ["decode_tc_kernel", "merge_dense_kernel"], "gpu_launches_per_step": 2,
+         "call_us": stats_us(ms), "latent_decode_kernel_us": stats_us(kms),
+         "dense_merge_us_median": round((pct(ms, 50) - pct(kms, 50)) * 1e3, 2),
+         "bytes": work["decode_bytes"] + dense_bytes, "flops": work["flops"],
+         "roofline": roofline_for(cfg, work, pct(ms, 50), peaks, peaks_src, long_step=False)}
+    e["roofline"]["duration"] = "median whole call (latent decode + dense merge)"
+    wl.close()
+    return e
+
+
 def run_next_rows(args, dev, flush, peaks, peaks_src):
     """The steps next to the decode kernel, each timed with CUDA events (L2 flushed before each
     launch) against its own roofline."""
@@ -640,6 +754,16 @@ def run_next_rows(args, dev, flush, peaks, peaks_src):
     for b in (1, 4):
         name = f"llama2-7b-oproj-fp16-b{b}"
         out[name] = bench_output_projection(args, dev, flush, peaks, peaks_src, b)
+        print(f"[bench] {name}: median {out[name]['kernel_us']['median']} us, frac {out[name]['roofline']['frac']}",
+              file=sys.stderr, flush=True)
+        torch.cuda.empty_cache()
+    out["llama2-7b-hybrid-int4-b4-t64k-s4-w64"] = bench_hybrid(args, dev, flush, peaks, peaks_src)
+    print(f"[bench] hybrid: call median {out['llama2-7b-hybrid-int4-b4-t64k-s4-w64']['call_us']['median']} us",
+          file=sys.stderr, flush=True)
+    torch.cuda.empty_cache()
+    for b, T, lat in ((1, 4096, "int4"), (4, 4096, "f16")):
+        name = f"llama2-7b-prefill-{lat}-b{b}-t4k"
+        out[name] = bench_prefill(args, dev, flush, peaks, peaks_src, b, T, lat)
         print(f"[bench] {name}: median {out[name]['kernel_us']['median']} us, frac {out[name]['roofline']['frac']}",
               file=sys.stderr, flush=True)
         torch.cuda.empty_cache()
