@@ -136,20 +136,36 @@ def decode_rope_head(q_i, hk_bg, hv_bg, bk_g, j: int, pos, qp: float, theta: flo
     return softmax_attend(scores, np.asarray(hv_bg, np.float64))
 
 
-def decode_absorbed_head(q_i, hk_bg, hv_bg, bk_g, j: int):
+def decode_absorbed_head(q_i, hk_bg, hv_bg, bk_g, j: int, bias=None):
     """One head of the non-RoPE path: the query is absorbed into the latent space,
     q'_i = q_i (B_i^k)^T, and scored straight against H_k
-    ([Palu] "方法细节", key fusion: q_i K_i^T = q_i (H_i^k B_i^k)^T = (q_i B_i^k^T) H_i^k^T)."""
+    ([Palu] "方法细节", key fusion: q_i K_i^T = q_i (H_i^k B_i^k)^T = (q_i B_i^k^T) H_i^k^T).
+    `bias` (one value per token) is added to the scores: a position bias that never touches
+    the keys, such as ALiBi's, leaves the key fusion valid (same paragraph)."""
     d_h = q_i.shape[-1]
     if hk_bg.shape[0] == 0:
         return np.zeros(hv_bg.shape[-1]), -math.inf
     q_lat = np.asarray(bk_g, np.float64)[:, j * d_h:(j + 1) * d_h] @ np.asarray(q_i, np.float64)
     scores = (np.asarray(hk_bg, np.float64) @ q_lat) / math.sqrt(d_h)
+    if bias is not None:
+        scores = scores + np.asarray(bias, np.float64)
     return softmax_attend(scores, np.asarray(hv_bg, np.float64))
 
 
+def alibi_slopes(n_heads: int) -> np.ndarray:
+    """ALiBi's per-head slopes m_i = 2^(-8 (i + 1) / n), the geometric sequence of the paper the
+    Palu notes cite for non-RoPE position encodings ("Train short, test long: attention with
+    linear biases"): 1/2, 1/4, ..., 1/256 for 8 heads."""
+    return np.power(2.0, -8.0 * (np.arange(n_heads, dtype=np.float64) + 1.0) / n_heads)
+
+
+def alibi_bias(slope: float, pos, qp: float) -> np.ndarray:
+    """The score bias of each key: -m (q_pos - pos_t), a penalty linear in the query's distance."""
+    return -slope * (float(qp) - np.asarray(pos, np.float64))
+
+
 def decode(q, hk, hv, bk, seq_lens, group_size: int, *, mode: str = "rope", theta: float = 10000.0,
-           positions=None, q_pos=None, heads=None):
+           positions=None, q_pos=None, heads=None, alibi: bool = False):
     """Decode attention for every (batch, head), or only for ``heads`` = [(b, i), ...].
 
     q  [B][n][d_h], hk [B][T][n_g][r_k], hv [B][T][n_g][r_v] (already dequantised),
@@ -171,7 +187,11 @@ def decode(q, hk, hv, bk, seq_lens, group_size: int, *, mode: str = "rope", thet
             qp = _query_position(positions, q_pos, b, T) if T > 0 else 0.0
             o[b, i], lse[b, i] = decode_rope_head(q[b, i], hk_bg, hv_bg, bk[g], j, pos, qp, theta)
         elif mode == "absorbed":
-            o[b, i], lse[b, i] = decode_absorbed_head(q[b, i], hk_bg, hv_bg, bk[g], j)
+            bias = None
+            if alibi and T > 0:
+                bias = alibi_bias(alibi_slopes(n)[i], _positions(positions, b, T),
+                                  _query_position(positions, q_pos, b, T))
+            o[b, i], lse[b, i] = decode_absorbed_head(q[b, i], hk_bg, hv_bg, bk[g], j, bias)
         else:
             raise ValueError(mode)
     return o, lse
@@ -242,7 +262,7 @@ def decode_hybrid(q, hk, hv, bk, seq_lens, group_size: int, dense_k, dense_v, n_
 # ---------------------------------------------------------------------------
 
 def mha_decode(q, x, wk, wv, seq_lens, *, theta: float = 10000.0, rope: bool = True,
-               positions=None, q_pos=None):
+               positions=None, q_pos=None, alibi: bool = False):
     """Plain MHA decode over cached activations x [B][T][d] ([Palu] "背景知识"):
     k_i = x W_i^k, v_i = x W_i^v, p = softmax(q_i K_i^T / sqrt(d_h)), a_i = p V_i.
     Returns a [B][n][d_h] and lse [B][n]."""
@@ -261,7 +281,10 @@ def mha_decode(q, x, wk, wv, seq_lens, *, theta: float = 10000.0, rope: bool = T
             if rope:
                 K = rope_rotate(K, pos, theta)
                 qi = rope_rotate(qi, qp, theta)
-            a[b, i], lse[b, i] = softmax_attend(K @ qi / math.sqrt(d_h), V)
+            sc = K @ qi / math.sqrt(d_h)
+            if alibi:
+                sc = sc + alibi_bias(alibi_slopes(n)[i], pos, qp)
+            a[b, i], lse[b, i] = softmax_attend(sc, V)
     return a, lse
 
 

@@ -52,7 +52,7 @@ def _rope_head_scale_r(q_i, hk_bg, hv_bg, bk_g, j, pos, qp, theta):
     return O.softmax_attend(s, hv_bg)
 
 
-def _absorbed_transposed(q_i, hk_bg, hv_bg, bk_g, j):
+def _absorbed_transposed(q_i, hk_bg, hv_bg, bk_g, j, bias=None):
     # uses the head's row block of B^T instead of its column block of B
     d_h = q_i.shape[-1]
     blk = bk_g[:, j * d_h:(j + 1) * d_h]
@@ -139,6 +139,11 @@ def _decode_hybrid_separate_softmax(q, hk, hv, bk, seq_lens, group_size, dense_k
     return o_lat, o_den, lse
 
 
+def _alibi_bias_wrong_sign(slope, pos, qp):
+    # rewards distance instead of penalising it
+    return slope * (float(qp) - np.asarray(pos, np.float64))
+
+
 ALL_PINS = [getattr(P, n) for n in dir(P) if n.startswith("test_")]
 
 MUTATIONS = {
@@ -156,6 +161,7 @@ MUTATIONS = {
     "project_rows_of_next_head": ("project_fused", _project_rows_of_next_head),
     "latents_first_group_only": ("project_latents", _project_latents_first_group),
     "hybrid_segments_normalised_apart": ("decode_hybrid", _decode_hybrid_separate_softmax),
+    "alibi_bias_wrong_sign": ("alibi_bias", _alibi_bias_wrong_sign),
 }
 
 

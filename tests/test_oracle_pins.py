@@ -512,3 +512,44 @@ def test_hybrid_with_an_empty_middle_is_dense_softmax_attention():
         np.testing.assert_allclose(o_den[0, i], scipy.special.softmax(sc) @ dv[0, :, i], atol=1e-13)
         assert abs(lse[0, i] - scipy.special.logsumexp(sc)) < 1e-13
     assert np.all(o_lat == 0)
+
+
+# ---------------------------------------------------------------------------
+# ALiBi on the absorbed path
+# ---------------------------------------------------------------------------
+
+def test_alibi_slopes_closed_form():
+    # the ALiBi paper's sequence for 8 heads is 1/2, 1/4, ..., 1/256; for 16 heads it starts at 2^-0.5
+    np.testing.assert_array_equal(O.alibi_slopes(8), [2.0 ** -k for k in range(1, 9)])
+    np.testing.assert_allclose(O.alibi_slopes(16)[:2], [2 ** -0.5, 0.5], rtol=1e-15)
+    assert O.alibi_bias(0.25, [0, 3, 7], 7).tolist() == [-1.75, -1.0, 0.0]
+
+
+def test_absorbed_alibi_at_full_rank_equals_mha_with_alibi():
+    # key fusion stays exact under a bias that never touches the keys
+    B, T, d, n, s, d_h = 2, 10, 32, 4, 2, 4
+    x, wk, wv, q = _mha_setup(51, B, T, d, n, s, d_h)
+    n_g, r = n // s, s * d_h
+    Ak, Bk = _group_factors(wk, n_g, s, d_h, r)
+    Av, Bv = _group_factors(wv, n_g, s, d_h, r)
+    hk = np.einsum("btd,gdr->btgr", x, Ak)
+    hv = np.einsum("btd,gdr->btgr", x, Av)
+    pos = np.stack([np.arange(T) * 3 + 5, np.arange(T)[::-1] + 2])
+    o, lse = O.decode(q, hk, hv, Bk, [T, T - 4], s, mode="absorbed", positions=pos, q_pos=[40, 30], alibi=True)
+    a, lse_ref = O.mha_decode(q, x, wk, wv, [T, T - 4], rope=False, positions=pos, q_pos=[40, 30], alibi=True)
+    for b in range(B):
+        for i in range(n):
+            g, j = i // s, i % s
+            np.testing.assert_allclose(o[b, i] @ Bv[g][:, j * d_h:(j + 1) * d_h], a[b, i], atol=1e-11)
+    np.testing.assert_allclose(lse, lse_ref, atol=1e-11)
+
+
+def test_alibi_depends_only_on_distance_and_changes_the_result():
+    q, hk, hv, bk = _tiny(seed=52, B=1, T=8, n=4, s=2, d_h=4, r=4, r_v=3)
+    pos = np.arange(8)[None]
+    o1, l1 = O.decode(q, hk, hv, bk, [8], 2, mode="absorbed", positions=pos, q_pos=[9], alibi=True)
+    o2, l2 = O.decode(q, hk, hv, bk, [8], 2, mode="absorbed", positions=pos + 100, q_pos=[109], alibi=True)
+    np.testing.assert_allclose(o1, o2, atol=1e-13)
+    np.testing.assert_allclose(l1, l2, atol=1e-13)
+    o0, _ = O.decode(q, hk, hv, bk, [8], 2, mode="absorbed")
+    assert np.abs(o1 - o0).max() > 1e-3
