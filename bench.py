@@ -70,10 +70,11 @@ def kv_bytes_dense(layers, kv_heads, head_dim, tokens, bytes_per_elem):
 
 def latent_bytes_per_token(cfg):
     """K + V latent bytes one token occupies across all groups of one layer."""
-    if cfg.latent_dtype == "int4":
-        return cfg.n_groups * ((cfg.rank // 2) * 2 + 2 * 2)  # codes + one fp16 scale each for K and V
-    elt = 4 if cfg.latent_dtype == "f32" else 2
-    return cfg.n_groups * 2 * cfg.rank * elt
+    def side(dtype):
+        if dtype == "int4":
+            return cfg.rank // 2 + 2                         # codes + one fp16 scale
+        return cfg.rank * (4 if dtype == "f32" else 2)
+    return cfg.n_groups * (side(cfg.latent_dtype) + side(cfg.value_dtype))
 
 
 def step_work(cfg):
@@ -274,7 +275,7 @@ class GpuWorkload:
     """Device-resident workload: the latent cache drawn on the device and filled through the
     append kernel one batch row at a time, plus the per-step inputs."""
 
-    def __init__(self, cfg, device, max_position=0):
+    def __init__(self, cfg, device, max_position=0, flags=0):
         import torch
         from rank_kv_cache_gb300 import palu as P
         from synthetic import gen
@@ -286,8 +287,8 @@ class GpuWorkload:
         self.attn = P.PaluAttention(self.bk_host.to(device), n_heads=cfg.n_heads, head_dim=cfg.head_dim,
                                     group_size=cfg.group_size, rank_k=r, rank_v=r, latent_dtype=lat,
                                     q_dtype=cfg.q_dtype, mode=cfg.mode, rope_theta=cfg.theta, max_batch=B,
-                                    max_tokens=T, max_position=max_position)
-        self.cache = P.LatentCache(B, T, n_g, r, r, lat, device=device)
+                                    max_tokens=T, max_position=max_position, v_dtype=cfg.value_dtype, flags=flags)
+        self.cache = P.LatentCache(B, T, n_g, r, r, lat, device=device, v_dtype=cfg.value_dtype)
         src_dt = "f32" if lat in ("int4", "f32") else lat
         tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[src_dt]
         zero = torch.zeros(1, dtype=torch.int32, device=device)
@@ -308,6 +309,7 @@ class GpuWorkload:
             c.hv += b * row_bytes_v
             if lat == "int4":
                 c.k_scale += b * T * n_g * 2
+            if cfg.value_dtype == "int4":
                 c.v_scale += b * T * n_g * 2
             P.check(P.palu_append_latents(self.attn.handle, c, hk.data_ptr(), hv.data_ptr(), P.DTYPES[src_dt],
                                           zero.data_ptr(), 1, T, int(torch.cuda.current_stream().cuda_stream)),
@@ -746,6 +748,38 @@ def bench_hybrid(args, dev, flush, peaks, peaks_src, sinks=4, window=64):
     return e
 
 
+VARIANTS = (
+    # name, workload base, overrides, descriptor flags
+    ("llama2-7b-rope-fp16k-int4v-b4-t64k", "ROPE_FP16", dict(batch=4, T=65536, v_dtype="int4"), 0),
+    ("llama2-7b-absorbed-alibi-fp16-b4-t64k", "ABSORBED_FP16", dict(), 1),
+    ("llama2-7b-rope-fp16-mlrd-s1-r64-b1-t4k", "ROPE_FP16", dict(group_size=1, rank=64), 0),
+    ("llama2-7b-rope-fp16-glrd-s2-r256-b1-t4k", "ROPE_FP16", dict(group_size=2), 0),
+    ("llama2-7b-rope-fp16-glrd-s4-r256-b1-t4k", "ROPE_FP16", dict(), 0),
+    ("llama2-7b-rope-fp16-glrd-s8-r256-b1-t4k", "ROPE_FP16", dict(group_size=8), 0),
+    ("llama2-7b-rope-fp16-jlrd-s32-r256-b1-t4k", "ROPE_FP16", dict(group_size=32), 0),
+)
+
+
+def bench_variant(args, dev, flush, peaks, peaks_src, base, over, flags):
+    """One decode variant at full size: append + decode steps, L2 flushed before each, the decode
+    kernel timed from the library's trace."""
+    import torch
+    from synthetic import gen
+    cfg = getattr(gen, base).with_(**over)
+    wl = GpuWorkload(cfg, dev, flags=flags)
+    for _ in range(5):
+        flush.zero_()
+        wl.step()
+    torch.cuda.synchronize()
+    step_ms, kms, clocks = timed_steps(wl, 50 if cfg.T > 4096 else 200, flush, dev.index)
+    work = step_work(cfg)
+    e = per_config_entry(f"variant:{base}", cfg, work, step_ms, kms, clocks, wl, peaks, peaks_src)
+    e.update({"group_size": cfg.group_size, "rank": cfg.rank, "value_dtype": cfg.value_dtype,
+              "alibi": bool(flags & 1), "rebuild_flops_per_token": work["flops"] // (cfg.batch * cfg.T)})
+    wl.close()
+    return e
+
+
 def run_next_rows(args, dev, flush, peaks, peaks_src):
     """The steps next to the decode kernel, each timed with CUDA events (L2 flushed before each
     launch) against its own roofline."""
@@ -756,6 +790,11 @@ def run_next_rows(args, dev, flush, peaks, peaks_src):
         out[name] = bench_output_projection(args, dev, flush, peaks, peaks_src, b)
         print(f"[bench] {name}: median {out[name]['kernel_us']['median']} us, frac {out[name]['roofline']['frac']}",
               file=sys.stderr, flush=True)
+        torch.cuda.empty_cache()
+    for name, base, over, flags in VARIANTS:
+        out[name] = bench_variant(args, dev, flush, peaks, peaks_src, base, over, flags)
+        print(f"[bench] {name}: decode kernel median {out[name]['decode_kernel_us']['median']} us, "
+              f"{out[name]['roofline']['bound']} frac {out[name]['roofline']['frac']}", file=sys.stderr, flush=True)
         torch.cuda.empty_cache()
     out["llama2-7b-hybrid-int4-b4-t64k-s4-w64"] = bench_hybrid(args, dev, flush, peaks, peaks_src)
     print(f"[bench] hybrid: call median {out['llama2-7b-hybrid-int4-b4-t64k-s4-w64']['call_us']['median']} us",

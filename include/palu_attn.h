@@ -90,11 +90,14 @@ typedef struct palu_attn_desc {
   int abi_version;        /* must be PALU_ABI_VERSION */
   int n_heads;            /* n */
   int head_dim;           /* d_h: 64 or 128 */
-  int group_size;         /* s: 1, 2, 4 or 8; n_heads % s == 0 */
+  int group_size;         /* s: 1, 2, 4 or 8 (M-LRD is s = 1); 16 or 32 (up to J-LRD, s = n) on the
+                             RoPE path with head_dim 128, ranks 256 and F16/BF16/INT4 latents
+                             ("方法细节", M-LRD / G-LRD / J-LRD paragraphs); n_heads % s == 0 */
   int rank_k;             /* r_k per group: 64, 128 or 256 */
   int rank_v;             /* r_v per group: 64, 128 or 256 */
   palu_dtype_t k_dtype;   /* key-latent storage */
-  palu_dtype_t v_dtype;   /* value-latent storage; this build requires v_dtype == k_dtype */
+  palu_dtype_t v_dtype;   /* value-latent storage: k_dtype, or PALU_INT4 under F16 / BF16 keys
+                             (int4 values only, the Palu notes' 4-bit V setting, "实验结果") */
   palu_dtype_t bk_dtype;  /* B_k storage: equals k_dtype, or PALU_F16 when k_dtype is PALU_INT4 */
   palu_dtype_t q_dtype;   /* query storage: F32, F16 or BF16 */
   palu_mode_t mode;
@@ -102,7 +105,7 @@ typedef struct palu_attn_desc {
   int max_batch;          /* largest batch any decode call will pass */
   int64_t max_tokens;     /* largest sequence length any decode call will see */
   int64_t max_position;   /* positions must lie in [0, max_position); 0 means max_tokens */
-  uint32_t flags;         /* 0, or PALU_FLAG_TEST_STALL (test builds of callers only) */
+  uint32_t flags;         /* 0, PALU_FLAG_ALIBI, or PALU_FLAG_TEST_STALL (test builds of callers only) */
 } palu_attn_desc;
 
 /*
@@ -114,6 +117,17 @@ typedef struct palu_attn_desc {
  * (palu_decode_plan tells which kernel a call uses). Never set it in production.
  */
 #define PALU_FLAG_TEST_STALL 0x80000000u
+
+/*
+ * ALiBi position bias on the absorbed path ("方法细节", key-fusion paragraph: a position
+ * encoding that never touches the keys, ALiBi being the example, leaves the absorbed query
+ * valid). Each score of head i gets -m_i (q_pos - pos_t) with the slopes m_i = 2^(-8 (i + 1) / n)
+ * of the ALiBi paper the notes cite; pos_t comes from `positions` (default t) and q_pos from
+ * `q_pos` (default the last cached token's position). Only with PALU_MODE_ABSORBED (else
+ * PALU_ERR_INVALID_ARG); palu_decode_attn_noalloc and palu_decode_hybrid take no positions and
+ * return PALU_ERR_UNSUPPORTED for it.
+ */
+#define PALU_FLAG_ALIBI 0x1u
 
 /*
  * A latent cache, caller-owned device memory. With n_g = n_heads / group_size:

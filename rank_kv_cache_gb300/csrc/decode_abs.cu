@@ -174,6 +174,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < 8; ++c) acc[j][c] = 0.f;
     float m_run[kHeads] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
     float l_run = 0.f;   // running sum of head (lane & 3) over this warp's tokens
+    // ALiBi: this lane's head (lane & 3) adds m (pos_t - q_pos) log2(e) to its scores
+    float alibi_m = 0.f, alibi_qp = 0.f;
+    if (a.alibi) {
+      alibi_m = exp2f(-8.f * float(head0 + (lane & 3) + 1) / float(a.n_heads)) * 1.4426950408889634f;
+      int qp = T > 0 ? (a.positions ? a.positions[(int64_t)b * a.capacity + T - 1] : T - 1) : 0;
+      if (a.q_pos) qp = a.q_pos[b];
+      alibi_qp = float(qp);
+    }
     bool broken = false;
     float* myp = pw + warp * 32;
 
@@ -206,7 +214,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // lane L now owns the score of token L / 4, head L % 4
       float sc = transpose_reduce32(part, lane);
       const int jl = lane & 3;
-      if (tok0 + (lane >> 2) >= t_end) sc = -INFINITY;
+      const int tk = tok0 + (lane >> 2);
+      if (a.alibi && tk < t_end) {
+        const int pos = a.positions ? a.positions[(int64_t)b * a.capacity + tk] : tk;
+        sc = fmaf(alibi_m, float(pos) - alibi_qp, sc);
+      }
+      if (tk >= t_end) sc = -INFINITY;
 
       // online softmax per head over this warp's tokens
       float bm = sc;

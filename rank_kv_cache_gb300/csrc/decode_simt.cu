@@ -141,6 +141,14 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(DecodeArgs a) {
         }
         sc += __shfl_xor_sync(0xffffffffu, sc, 1);
         sc += __shfl_xor_sync(0xffffffffu, sc, 2);
+        if (a.alibi && pr < TT * s && t < nt) {
+          // ALiBi: m_i (pos_t - q_pos) log2(e), m_i = 2^(-8 (i + 1) / n) for head i = g s + j
+          const int pos = a.positions ? a.positions[(int64_t)b * a.capacity + t0 + t] : t0 + t;
+          int qp = a.positions ? a.positions[(int64_t)b * a.capacity + T - 1] : T - 1;
+          if (a.q_pos) qp = a.q_pos[b];
+          const float m = exp2f(-8.f * float(g * s + j + 1) / float(a.n_heads)) * 1.4426950408889634f;
+          sc = fmaf(m, float(pos) - float(qp), sc);
+        }
         if (pr < TT * s && part == 0) sc_s[t * s + j] = (t < nt) ? sc : -INFINITY;
       }
     }
@@ -223,8 +231,11 @@ cudaError_t launch_t(const DecodeArgs& a, cudaStream_t st) {
 template <int MODE>
 cudaError_t launch_mode(const DecodeArgs& a, cudaStream_t st) {
   if (a.k_dtype == kF32) return launch_t<MODE, float, float, float>(a, st);
-  if (a.k_dtype == kF16) return launch_t<MODE, __half, __half, __half>(a, st);
-  if (a.k_dtype == kBF16) return launch_t<MODE, __nv_bfloat16, __nv_bfloat16, __nv_bfloat16>(a, st);
+  if (a.k_dtype == kF16)
+    return a.v_dtype == kINT4 ? launch_t<MODE, __half, Int4, __half>(a, st) : launch_t<MODE, __half, __half, __half>(a, st);
+  if (a.k_dtype == kBF16)
+    return a.v_dtype == kINT4 ? launch_t<MODE, __nv_bfloat16, Int4, __nv_bfloat16>(a, st)
+                              : launch_t<MODE, __nv_bfloat16, __nv_bfloat16, __nv_bfloat16>(a, st);
   return launch_t<MODE, Int4, Int4, __half>(a, st);
 }
 

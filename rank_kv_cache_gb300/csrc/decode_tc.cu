@@ -36,6 +36,7 @@
 #include <cuda.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "internal.h"
 #include "split_merge.cuh"
@@ -61,23 +62,24 @@ constexpr uint32_t kTmemCols = 512;              // two N=256 fp32 accumulators
 
 constexpr float kTurnToRad = 1.4629180792671596e-09f;  // 2 pi / 2^32
 
-// Per-variant layout. I4 = int4 latents: the H_k tile arrives packed (16 KB) and a converter
-// warpgroup expands it into the fp16 operand ring; H_v chunks hold packed rows.
+// Per-variant layout. I4K = int4 key latents: the H_k tile arrives packed (16 KB) and a converter
+// warpgroup expands it into the fp16 operand ring. I4V = int4 value latents: H_v chunks hold
+// packed rows (64 tokens each) for the dp2a p H_v.
 // Warpgroups: 0 = warp 0 H_k/B producer, warp 1 MMA issuer, warp 2 H_v producer, warp 3 idle;
 // 1, 2 = score warpgroups (rotation pairs 0-31 / 32-63); 3, 4 = softmax/PV warpgroups
-// (value columns 0-127 / 128-255); 5 = int4 converter (I4 only).
-template <bool I4>
+// (value columns 0-127 / 128-255); 5 = int4 key converter (I4K only).
+template <bool I4K, bool I4V>
 struct Lay {
-  static constexpr int kThreads = (I4 ? 6 : 5) * kWg;
-  static constexpr int kLaunchRegs = I4 ? 80 : 96;  // per thread at launch (launch bounds, one CTA per SM)
-  static constexpr int kRegsCtl = I4 ? 40 : 48, kRegsScore = I4 ? 128 : 152, kRegsPv = 64, kRegsConv = 48;
-  static constexpr int kStages = I4 ? 2 : 3;        // fp16 H_k operand ring
-  static constexpr int kPStages = I4 ? 2 : 0;       // packed int4 H_k tiles
+  static constexpr int kThreads = (I4K ? 6 : 5) * kWg;
+  static constexpr int kLaunchRegs = I4K ? 80 : 96;  // per thread at launch (launch bounds, one CTA per SM)
+  static constexpr int kRegsCtl = I4K ? 40 : 48, kRegsScore = I4K ? 128 : 152, kRegsPv = 64, kRegsConv = 48;
+  static constexpr int kStages = I4K ? 2 : 3;        // fp16 H_k operand ring
+  static constexpr int kPStages = I4K ? 2 : 0;       // packed int4 H_k tiles
   static constexpr int kPStage = kTile * (kRank / 2);
-  static constexpr int kVTok = I4 ? 64 : 16;        // tokens per H_v chunk
-  static constexpr int kVRow = I4 ? kRank / 2 : kRank * 2;
+  static constexpr int kVTok = I4V ? 64 : 16;        // tokens per H_v chunk
+  static constexpr int kVRow = I4V ? kRank / 2 : kRank * 2;
   static constexpr int kVSlot = kVTok * kVRow;      // 8 KB
-  static constexpr int kVSlots = I4 ? 2 : 5;
+  static constexpr int kVSlots = I4V ? (I4K ? 2 : 4) : 5;
   static constexpr int kVChunks = kTile / kVTok;
   static constexpr int kOffB = 0;
   static constexpr int kOffA = kOffB + kBBytes;
@@ -95,7 +97,7 @@ struct Lay {
   static constexpr int kSmemBytes = kOffL + 2 * 4 * 8;
   static constexpr int kSmemAlloc = kSmemBytes + 1024;
   static constexpr int kOffO = kOffV;                          // [8 warps][kHeads][kRank] floats
-  static_assert(kWg * kRegsCtl + 2 * kWg * kRegsScore + 2 * kWg * kRegsPv + (I4 ? kWg * kRegsConv : 0) <=
+  static_assert(kWg * kRegsCtl + 2 * kWg * kRegsScore + 2 * kWg * kRegsPv + (I4K ? kWg * kRegsConv : 0) <=
                     kThreads * kLaunchRegs,
                 "register split");
   static_assert(8 * kHeads * kRank * 4 <= kVSlots * kVSlot, "output reduction fits the H_v ring");
@@ -283,13 +285,14 @@ __device__ __forceinline__ void setmaxnreg_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
-// VT = value-latent storage (__half, __nv_bfloat16, or Int4); I4 = int4 latents (fp16 MMA operands);
+// VT = value-latent storage (__half, __nv_bfloat16, or Int4); I4K = int4 key latents (fp16 MMA operands);
 // FOLD = the rotated query is folded into the B operand (fp16 operands only, see below)
-template <typename VT, bool I4, bool FOLD>
-__global__ void __launch_bounds__(Lay<I4>::kThreads, 1)
+template <typename VT, bool I4K, bool FOLD>
+__global__ void __launch_bounds__(Lay<I4K, std::is_same<VT, Int4>::value>::kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_hk, const __grid_constant__ CUtensorMap tm_hv,
                      const __grid_constant__ CUtensorMap tm_b, const TcParams P) {
-  using LY = Lay<I4>;
+  constexpr bool I4V = std::is_same<VT, Int4>::value;   // int4 value latents (dp2a p H_v)
+  using LY = Lay<I4K, I4V>;
   constexpr int kStages = LY::kStages, kPStages = LY::kPStages, kVSlots = LY::kVSlots, kVTok = LY::kVTok;
   constexpr int kVChunks = LY::kVChunks, kVSlot = LY::kVSlot, kVRow = LY::kVRow;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -336,7 +339,7 @@ __global__ void __launch_bounds__(Lay<I4>::kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      tc::mbar_init(&fullA[i], I4 ? 4 : 1);   // converter warps, or the TMA
+      tc::mbar_init(&fullA[i], I4K ? 4 : 1);   // converter warps, or the TMA
       tc::mbar_init(&emptyA[i], 1);
     }
     for (int i = 0; i < kChunks; ++i) tc::mbar_init(&bfull[i], 1);
@@ -368,7 +371,7 @@ __global__ void __launch_bounds__(Lay<I4>::kThreads, 1)
         tc::mbar_arrive_expect_tx(&bfull[kc], kBChunk);
         tc::tma_load_2d(smem + LY::kOffB + kc * kBChunk, &tm_b, &bfull[kc], kc * kKChunk, brow);
       }
-      if constexpr (I4) {
+      if constexpr (I4K) {
         for (int it = 0; it < min(kPStages, n_tiles); ++it) {
           tc::mbar_arrive_expect_tx(&pfull[it], LY::kPStage);
           tc::tma_load_3d(smem + LY::kOffPk + it * LY::kPStage, &tm_hk, &pfull[it], 0, g, row0 + t_begin + it * kTile);
@@ -419,7 +422,7 @@ __global__ void __launch_bounds__(Lay<I4>::kThreads, 1)
       if (lane == 0 && n_tiles > 0) {
         // B_k^T and the first ring fills were issued in the prologue
         bool ok = true;
-        if constexpr (I4) {
+        if constexpr (I4K) {
           // whole packed tiles (128 tokens x 128 bytes) into the staging ring
           int issued = min(kPStages, n_tiles);
           for (int it = issued; it < n_tiles && ok; ++it) {
@@ -554,7 +557,7 @@ __global__ void __launch_bounds__(Lay<I4>::kThreads, 1)
     bool slot_lost = false;   // warp-uniform: a score-slot wait gave up
     int pos_next = token_position(a, b, t_begin + row, t_begin + row < t_end);
     float ks_next = 1.f;
-    if constexpr (I4)
+    if constexpr (I4K)
       if (t_begin + row < t_end) ks_next = __half2float(a.k_scale[((int64_t)row0 + t_begin + row) * a.n_g + g]);
     for (int it = 0; it < n_tiles; ++it) {
       const int buf = it & 1;
@@ -566,7 +569,7 @@ __global__ void __launch_bounds__(Lay<I4>::kThreads, 1)
       if (it + 1 < n_tiles) {
         const int tn = t0 + kTile + row;
         pos_next = token_position(a, b, tn, tn < t_end);
-        if constexpr (I4)
+        if constexpr (I4K)
           if (tn < t_end) ks_next = __half2float(a.k_scale[((int64_t)row0 + tn) * a.n_g + g]);
       }
 
@@ -657,7 +660,7 @@ __global__ void __launch_bounds__(Lay<I4>::kThreads, 1)
       if (!fold_b(smem + LY::kOffB, qs, bfull, bready, threadIdx.x - kWg, lane, abort_flag, kWaitNs)) broken = true;
     }
     float vs_next = 1.f;
-    if constexpr (I4)
+    if constexpr (I4V)
       if (t_begin + ei < t_end) vs_next = __half2float(a.v_scale[((int64_t)row0 + t_begin + ei) * a.n_g + g]);
 
     for (int it = 0; it < n_tiles; ++it) {
@@ -665,7 +668,7 @@ __global__ void __launch_bounds__(Lay<I4>::kThreads, 1)
       const uint32_t use = it >> 1;
       const int t0 = t_begin + it * kTile;
       const float vsc = vs_next;
-      if constexpr (I4)
+      if constexpr (I4V)
         if (it + 1 < n_tiles && t0 + kTile + ei < t_end)
           vs_next = __half2float(a.v_scale[((int64_t)row0 + t0 + kTile + ei) * a.n_g + g]);
       const bool got = tc::mbar_wait_bounded(&sready[buf], use & 1, abort_flag, kWaitNs);
@@ -698,7 +701,7 @@ __global__ void __launch_bounds__(Lay<I4>::kThreads, 1)
       m_run1 = mn1;
       l0 = l0 * al0 + p0;
       l1 = l1 * al1 + p1;
-      pbuf[ei] = I4 ? make_float2(p0 * vsc, p1 * vsc) : make_float2(p0, p1);
+      pbuf[ei] = I4V ? make_float2(p0 * vsc, p1 * vsc) : make_float2(p0, p1);
       tc::named_bar(bar, kWg);
 
       {
@@ -709,7 +712,7 @@ __global__ void __launch_bounds__(Lay<I4>::kThreads, 1)
           acc1[c] = __fmul2_rn(acc1[c], a1);
         }
       }
-      if constexpr (I4) {
+      if constexpr (I4V) {
         // p H_v on the integer codes. Warp w8 owns tokens 64 ch + 8 w8 .. 64 ch + 8 w8 + 7 of
         // chunks ch = 0, 1 (16 tokens); lane l quantises the weight p' = p * v_scale of token
         // (l & 15) for head l >> 4 to 15 bits against the largest of the warp's 16 weights of that
@@ -822,10 +825,10 @@ __global__ void __launch_bounds__(Lay<I4>::kThreads, 1)
       }
     }
   } else {
-    // ------------------------------------------------------------ int4 converter (I4 only)
+    // ------------------------------------------------------------ int4 key converter (I4K only)
     // thread = one token row: expand the row's packed codes into exact fp16 codes in the MMA
     // operand ring (128-byte swizzle, one 64-column chunk per stage).
-    if constexpr (I4) {
+    if constexpr (I4K) {
       setmaxnreg_dec<LY::kRegsConv>();
       const int r = threadIdx.x - 5 * kWg;
       bool ok = true;
@@ -898,8 +901,11 @@ bool tma_encode(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* ba
 
 bool tc_supported(const DecodeArgs& a) {
   const bool i4 = a.k_dtype == kINT4;
-  return (a.k_dtype == kF16 || a.k_dtype == kBF16 || i4) && a.v_dtype == a.k_dtype &&
-         (!i4 || a.bk_dtype == kF16) && a.dh == kDh && a.rk == kRank && a.rv == kRank && a.s % kHeads == 0 &&
+  // key and value latents of one dtype, or fp16 / bf16 keys with int4 values (V-only int4)
+  const bool types = (a.k_dtype == kF16 || a.k_dtype == kBF16 || i4) &&
+                     (a.v_dtype == a.k_dtype || (!i4 && a.v_dtype == kINT4));
+  return types && (!i4 || a.bk_dtype == kF16) && a.dh == kDh && a.rk == kRank && a.rv == kRank &&
+         a.s % kHeads == 0 &&
          (int64_t)a.batch * a.capacity >= kTile && (int64_t)a.batch * a.capacity < (int64_t(1) << 31) &&
          encode_fn() != nullptr;
 }
@@ -907,50 +913,55 @@ bool tc_supported(const DecodeArgs& a) {
 int tc_tile_tokens() { return kTile; }
 int tc_ctas_per_group(const DecodeArgs& a) { return a.s / kHeads; }
 
-template <typename VT, bool I4, bool FOLD>
+template <typename VT, bool I4K, bool FOLD>
 cudaError_t launch_variant(const CUtensorMap& tm_hk, const CUtensorMap& tm_hv, const CUtensorMap& tm_b,
                            const TcParams& P, cudaStream_t st) {
-  auto kern = decode_tc_kernel<VT, I4, FOLD>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<I4>::kSmemAlloc);
+  using LY = Lay<I4K, std::is_same<VT, Int4>::value>;
+  auto kern = decode_tc_kernel<VT, I4K, FOLD>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::kSmemAlloc);
   if (e != cudaSuccess) return e;
   dim3 grid(P.a.n_splits * P.hp_count, P.a.n_g, P.a.batch);
-  kern<<<grid, Lay<I4>::kThreads, Lay<I4>::kSmemAlloc, st>>>(tm_hk, tm_hv, tm_b, P);
+  kern<<<grid, LY::kThreads, LY::kSmemAlloc, st>>>(tm_hk, tm_hv, tm_b, P);
   return cudaGetLastError();
 }
 
 cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st) {
   if (!encode_fn()) return cudaErrorNotSupported;
-  const bool i4 = a.k_dtype == kINT4;
+  const bool i4k = a.k_dtype == kINT4, i4v = a.v_dtype == kINT4;
   const CUtensorMapDataType dt = a.k_dtype == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUtensorMap tm_hk, tm_hv, tm_b;
   const cuuint64_t rows = (cuuint64_t)a.batch * a.capacity;
-  if (i4) {
-    // packed rows [rows][n_g][r/2] bytes: H_k as whole 128-token tiles (128-byte swizzle for the
-    // converter's row reads), H_v as 64-token chunks
-    const cuuint64_t dims[3] = {(cuuint64_t)kRank / 2, (cuuint64_t)a.n_g, rows};
-    const cuuint64_t strides[2] = {(cuuint64_t)kRank / 2, (cuuint64_t)a.n_g * (kRank / 2)};
+  // packed int4 rows [rows][n_g][r/2] bytes; fp16 / bf16 rows [rows][n_g][r]
+  const cuuint64_t pdims[3] = {(cuuint64_t)kRank / 2, (cuuint64_t)a.n_g, rows};
+  const cuuint64_t pstrides[2] = {(cuuint64_t)kRank / 2, (cuuint64_t)a.n_g * (kRank / 2)};
+  const cuuint64_t fdims[3] = {(cuuint64_t)kRank, (cuuint64_t)a.n_g, rows};
+  const cuuint64_t fstrides[2] = {(cuuint64_t)kRank * 2, (cuuint64_t)a.n_g * kRank * 2};
+  if (i4k) {
+    // H_k as whole 128-token packed tiles, 128-byte swizzle for the converter's row reads
     const cuuint32_t boxk[3] = {kRank / 2, 1, kTile};
-    const cuuint32_t boxv[3] = {kRank / 2, 1, (cuuint32_t)Lay<true>::kVTok};
-    if (!encode(&tm_hk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, a.hk, dims, strides, boxk, CU_TENSOR_MAP_SWIZZLE_128B))
-      return cudaErrorInvalidValue;
-    if (!encode(&tm_hv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, a.hv, dims, strides, boxv, CU_TENSOR_MAP_SWIZZLE_NONE))
+    if (!encode(&tm_hk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, a.hk, pdims, pstrides, boxk, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   } else {
-    // H_k as [rows][n_g][r]: boxes of 64 ranks x 1 group x 128 tokens, 128-byte swizzle (MMA operand)
-    const cuuint64_t dims[3] = {(cuuint64_t)a.rk, (cuuint64_t)a.n_g, rows};
-    const cuuint64_t strides[2] = {(cuuint64_t)a.rk * 2, (cuuint64_t)a.n_g * a.rk * 2};
+    // H_k as boxes of 64 ranks x 1 group x 128 tokens, 128-byte swizzle (the MMA operand)
     const cuuint32_t boxk[3] = {kKChunk, 1, kTile};
-    if (!encode(&tm_hk, dt, 3, a.hk, dims, strides, boxk, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
-    // H_v: whole 512-byte rows x 16 tokens, unswizzled (row reads)
-    const cuuint32_t boxv[3] = {(cuuint32_t)kRank, 1, (cuuint32_t)Lay<false>::kVTok};
-    if (!encode(&tm_hv, dt, 3, a.hv, dims, strides, boxv, CU_TENSOR_MAP_SWIZZLE_NONE)) return cudaErrorInvalidValue;
+    if (!encode(&tm_hk, dt, 3, a.hk, fdims, fstrides, boxk, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+  }
+  if (i4v) {
+    // H_v as 64-token chunks of packed rows, unswizzled (row reads)
+    const cuuint32_t boxv[3] = {kRank / 2, 1, 64};
+    if (!encode(&tm_hv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, a.hv, pdims, pstrides, boxv, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+  } else {
+    // H_v as whole 512-byte rows x 16 tokens, unswizzled (row reads)
+    const cuuint32_t boxv[3] = {(cuuint32_t)kRank, 1, 16};
+    if (!encode(&tm_hv, dt, 3, a.hv, fdims, fstrides, boxv, CU_TENSOR_MAP_SWIZZLE_NONE)) return cudaErrorInvalidValue;
   }
   {
     // B_k^T as [n_g * s * d_h][r]: boxes of 64 ranks x 256 rows, 128-byte swizzle
     const cuuint64_t dims[2] = {(cuuint64_t)a.rk, (cuuint64_t)a.n_g * a.s * a.dh};
     const cuuint64_t strides[1] = {(cuuint64_t)a.rk * 2};
     const cuuint32_t box[2] = {kKChunk, kN};
-    if (!encode(&tm_b, i4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : dt, 2, a.bkt, dims, strides, box,
+    if (!encode(&tm_b, i4k ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : dt, 2, a.bkt, dims, strides, box,
                 CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
@@ -960,9 +971,12 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, cudaStream_t st) {
   P.bf16 = a.k_dtype == kBF16;
   // fp16 operands carry the folded query with 11-bit precision; bf16 ones (8-bit) would not,
   // so the bf16 kernel rebuilds K exactly and applies the query in the epilogue
-  if (i4) return launch_variant<Int4, true, true>(tm_hk, tm_hv, tm_b, P, st);
-  if (a.k_dtype == kBF16) return launch_variant<__nv_bfloat16, false, false>(tm_hk, tm_hv, tm_b, P, st);
-  return launch_variant<__half, false, true>(tm_hk, tm_hv, tm_b, P, st);
+  if (i4k) return launch_variant<Int4, true, true>(tm_hk, tm_hv, tm_b, P, st);
+  if (a.k_dtype == kBF16)
+    return i4v ? launch_variant<Int4, false, false>(tm_hk, tm_hv, tm_b, P, st)
+               : launch_variant<__nv_bfloat16, false, false>(tm_hk, tm_hv, tm_b, P, st);
+  return i4v ? launch_variant<Int4, false, true>(tm_hk, tm_hv, tm_b, P, st)
+             : launch_variant<__half, false, true>(tm_hk, tm_hv, tm_b, P, st);
 }
 
 // ---------------------------------------------------------------------------- int4 test exports

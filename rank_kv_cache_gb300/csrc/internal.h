@@ -54,6 +54,8 @@ struct DecodeArgs {
   // producer issues nothing; wait_ns bounds every mbarrier wait of that kernel
   int test_stall;
   uint64_t wait_ns;
+  // ALiBi (absorbed path): every score of head i gets m_i (pos_t - q_pos), m_i = 2^(-8 (i + 1) / n)
+  int alibi;
 };
 
 // create-time set-up
@@ -68,8 +70,8 @@ cudaError_t launch_decode_simt(int mode, const DecodeArgs& a, cudaStream_t st);
 cudaError_t launch_combine(const DecodeArgs& a, float* out, float* lse, cudaStream_t st);
 // append the new tokens' key and value latents in one launch
 cudaError_t launch_append(void* cache_k, __half* scale_k, int rank_k, const void* src_k, void* cache_v,
-                          __half* scale_v, int rank_v, const void* src_v, int cache_dtype, int64_t capacity, int n_g,
-                          int src_dtype, const int32_t* dst_slot, int batch, int n_new, ErrWord* err,
+                          __half* scale_v, int rank_v, const void* src_v, int k_dtype, int v_dtype, int64_t capacity,
+                          int n_g, int src_dtype, const int32_t* dst_slot, int batch, int n_new, ErrWord* err,
                           cudaStream_t st);
 cudaError_t launch_debug_dequant(const void* cache, const __half* scale, int cache_dtype, int64_t capacity,
                                  int n_g, int rank, int batch, int64_t n_tokens, float* out, cudaStream_t st);

@@ -31,17 +31,25 @@ palu_status_t check_desc(const palu_attn_desc* d) {
   if (d->n_heads <= 0 || d->group_size <= 0 || d->n_heads % d->group_size != 0) return PALU_ERR_INVALID_ARG;
   if (d->max_batch <= 0 || d->max_tokens <= 0 || d->max_position < 0) return PALU_ERR_INVALID_ARG;
   if (d->max_tokens > (int64_t)1 << 30 || d->max_position > (int64_t)1 << 30) return PALU_ERR_INVALID_ARG;
-  if ((d->flags & ~PALU_FLAG_TEST_STALL) != 0) return PALU_ERR_INVALID_ARG;
+  if ((d->flags & ~(PALU_FLAG_TEST_STALL | PALU_FLAG_ALIBI)) != 0) return PALU_ERR_INVALID_ARG;
   if (d->mode != PALU_MODE_ROPE && d->mode != PALU_MODE_ABSORBED) return PALU_ERR_INVALID_ARG;
+  if ((d->flags & PALU_FLAG_ALIBI) && d->mode != PALU_MODE_ABSORBED) return PALU_ERR_INVALID_ARG;
   if ((unsigned)d->k_dtype > PALU_INT4 || (unsigned)d->v_dtype > PALU_INT4) return PALU_ERR_INVALID_ARG;
   if ((unsigned)d->bk_dtype > PALU_BF16 || (unsigned)d->q_dtype > PALU_BF16) return PALU_ERR_INVALID_ARG;
   if (d->mode == PALU_MODE_ROPE && !(d->rope_theta > 0.0 && isfinite(d->rope_theta))) return PALU_ERR_INVALID_ARG;
   if (d->head_dim <= 0 || d->rank_k <= 0 || d->rank_v <= 0) return PALU_ERR_INVALID_ARG;
   // shapes and type combinations with a kernel in this build
   if (d->head_dim != 64 && d->head_dim != 128) return PALU_ERR_UNSUPPORTED;
-  if (!pow2_in(d->group_size, 1, 8)) return PALU_ERR_UNSUPPORTED;
+  // group sizes 1..8 run on every path; 16 and 32 (joint decomposition of up to all 32 heads of a
+  // Llama-2-7B layer) only on the tensor-core RoPE kernel, whose shape rules they must meet
+  const bool tc_shape = d->mode == PALU_MODE_ROPE && d->head_dim == 128 && d->rank_k == 256 && d->rank_v == 256 &&
+                        (d->k_dtype == PALU_F16 || d->k_dtype == PALU_BF16 || d->k_dtype == PALU_INT4);
+  if (!pow2_in(d->group_size, 1, 8) && !(tc_shape && (d->group_size == 16 || d->group_size == 32)))
+    return PALU_ERR_UNSUPPORTED;
   if (!pow2_in(d->rank_k, 64, 256) || !pow2_in(d->rank_v, 64, 256)) return PALU_ERR_UNSUPPORTED;
-  if (d->v_dtype != d->k_dtype) return PALU_ERR_UNSUPPORTED;
+  // one latent dtype for keys and values, or int4 values under fp16 / bf16 keys (V-only int4)
+  if (d->v_dtype != d->k_dtype && !(d->v_dtype == PALU_INT4 && (d->k_dtype == PALU_F16 || d->k_dtype == PALU_BF16)))
+    return PALU_ERR_UNSUPPORTED;
   const palu_dtype_t want_bk = d->k_dtype == PALU_INT4 ? PALU_F16 : d->k_dtype;
   if (d->bk_dtype != want_bk) return PALU_ERR_UNSUPPORTED;
   return PALU_OK;
@@ -308,8 +316,8 @@ palu_status_t palu_append_latents(palu_attn_t h, const palu_cache* cache, const 
   ErrWord* err = reinterpret_cast<ErrWord*>(h->ws + h->L.err);
   const cudaError_t e = launch_append(cache->hk, static_cast<__half*>(cache->k_scale), h->d.rank_k, hk_new,
                                       cache->hv, static_cast<__half*>(cache->v_scale), h->d.rank_v, hv_new,
-                                      to_dt(h->d.k_dtype), cache->capacity, h->n_g, to_dt(src_dtype), dst_slot, batch,
-                                      n_new, err, s);
+                                      to_dt(h->d.k_dtype), to_dt(h->d.v_dtype), cache->capacity, h->n_g,
+                                      to_dt(src_dtype), dst_slot, batch, n_new, err, s);
   return e == cudaSuccess ? PALU_OK : PALU_ERR_CUDA;
 }
 
@@ -413,6 +421,7 @@ static void fill_args(const palu_attn* h, const palu_cache* cache, int batch, in
   a.err = reinterpret_cast<ErrWord*>(h->ws + h->L.err);
   a.counters = reinterpret_cast<unsigned*>(h->ws + h->L.counters);  // the decode kernels merge the splits
   a.test_stall = (d.flags & PALU_FLAG_TEST_STALL) ? 1 : 0;
+  a.alibi = (d.flags & PALU_FLAG_ALIBI) ? 1 : 0;
   a.wait_ns = a.test_stall ? 50000000ull : 1000000000ull;   // bound of every device wait
 }
 
@@ -470,7 +479,7 @@ palu_status_t palu_decode_attn(palu_attn_t h, const void* q, const palu_cache* c
   DecodeArgs a{};
   fill_args(h, cache, batch, max_seq_len, a);
   a.seq_lens = seq_lens;
-  a.positions = (h->d.mode == PALU_MODE_ROPE) ? positions : nullptr;
+  a.positions = (h->d.mode == PALU_MODE_ROPE || (h->d.flags & PALU_FLAG_ALIBI)) ? positions : nullptr;
   a.q = q;
   a.q_pos = q_pos;
   a.out = out;
@@ -478,6 +487,8 @@ palu_status_t palu_decode_attn(palu_attn_t h, const void* q, const palu_cache* c
   const int mode = h->d.mode == PALU_MODE_ROPE ? kRope : kAbsorbed;
   const int kernel = plan_decode(h, a);
   const bool use_tc = kernel == PALU_KERNEL_TC_ROPE, use_abs = kernel == PALU_KERNEL_TMA_ABSORBED;
+  // group sizes above 8 have no CUDA-core kernel (a cache of fewer than 128 rows in all)
+  if (kernel == PALU_KERNEL_SIMT && h->d.group_size > 8) return PALU_ERR_UNSUPPORTED;
 
   // the tensor-core kernel rotates its query itself; the other kernels read the prepared buffer
   cudaError_t e = use_tc ? cudaSuccess
@@ -495,6 +506,7 @@ palu_status_t palu_decode_hybrid(palu_attn_t h, const void* q, const palu_cache*
                                  const palu_dense_cache* dense, float* out, float* out_dense, float* lse,
                                  palu_stream_t stream) {
   if (!h || !dense) return PALU_ERR_INVALID_ARG;
+  if (h->d.flags & PALU_FLAG_ALIBI) return PALU_ERR_UNSUPPORTED;   // the dense tokens carry no positions
   if (h->d.head_dim > 128 || h->d.head_dim % 32) return PALU_ERR_UNSUPPORTED;
   if (batch < 0 || batch > h->d.max_batch) return PALU_ERR_INVALID_ARG;
   if (batch == 0) return PALU_OK;

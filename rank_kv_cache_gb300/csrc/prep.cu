@@ -204,11 +204,13 @@ struct AppendSide {
   __half* scale;
   const void* src;
   int rank;
+  int dtype;   // this side's cache dtype (values may be int4 while keys are not)
 };
 
-__device__ void append_row(const AppendSide& sd, int cache_dtype, int64_t capacity, int n_g, int src_dtype,
-                           const int32_t* dst_slot, int n_new, int64_t row, int lane, ErrWord* err) {
+__device__ void append_row(const AppendSide& sd, int64_t capacity, int n_g, int src_dtype, const int32_t* dst_slot,
+                           int n_new, int64_t row, int lane, ErrWord* err) {
   const int rank = sd.rank;
+  const int cache_dtype = sd.dtype;
   const int g = int(row % n_g);
   const int i = int((row / n_g) % n_new);
   const int b = int(row / ((int64_t)n_g * n_new));
@@ -288,27 +290,27 @@ __device__ void append_row(const AppendSide& sd, int cache_dtype, int64_t capaci
 
 // One warp per (side, b, new token, group) row; rows of the key cache come first, then the
 // value cache, so both are written by one launch.
-__global__ void append_kernel(AppendSide k_side, AppendSide v_side, int cache_dtype, int64_t capacity, int n_g,
-                              int src_dtype, const int32_t* dst_slot, int batch, int n_new, ErrWord* err) {
+__global__ void append_kernel(AppendSide k_side, AppendSide v_side, int64_t capacity, int n_g, int src_dtype,
+                              const int32_t* dst_slot, int batch, int n_new, ErrWord* err) {
   const int warps = blockDim.x / 32;
   const int64_t gw = (int64_t)blockIdx.x * warps + threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
   const int64_t rows = (int64_t)batch * n_new * n_g;
   if (gw >= 2 * rows) return;
-  if (gw < rows) append_row(k_side, cache_dtype, capacity, n_g, src_dtype, dst_slot, n_new, gw, lane, err);
-  else append_row(v_side, cache_dtype, capacity, n_g, src_dtype, dst_slot, n_new, gw - rows, lane, err);
+  if (gw < rows) append_row(k_side, capacity, n_g, src_dtype, dst_slot, n_new, gw, lane, err);
+  else append_row(v_side, capacity, n_g, src_dtype, dst_slot, n_new, gw - rows, lane, err);
 }
 
 cudaError_t launch_append(void* cache_k, __half* scale_k, int rank_k, const void* src_k, void* cache_v,
-                          __half* scale_v, int rank_v, const void* src_v, int cache_dtype, int64_t capacity, int n_g,
-                          int src_dtype, const int32_t* dst_slot, int batch, int n_new, ErrWord* err,
+                          __half* scale_v, int rank_v, const void* src_v, int k_dtype, int v_dtype, int64_t capacity,
+                          int n_g, int src_dtype, const int32_t* dst_slot, int batch, int n_new, ErrWord* err,
                           cudaStream_t st) {
   const int64_t rows = (int64_t)batch * n_new * n_g;
   if (rows == 0) return cudaSuccess;
   const int warps = 8;
   const int64_t blocks = (2 * rows + warps - 1) / warps;
-  append_kernel<<<(unsigned)blocks, warps * 32, 0, st>>>(AppendSide{cache_k, scale_k, src_k, rank_k},
-                                                          AppendSide{cache_v, scale_v, src_v, rank_v}, cache_dtype,
+  append_kernel<<<(unsigned)blocks, warps * 32, 0, st>>>(AppendSide{cache_k, scale_k, src_k, rank_k, k_dtype},
+                                                          AppendSide{cache_v, scale_v, src_v, rank_v, v_dtype},
                                                           capacity, n_g, src_dtype, dst_slot, batch, n_new, err);
   return cudaGetLastError();
 }

@@ -24,6 +24,7 @@ PALU_F32, PALU_F16, PALU_BF16, PALU_INT4 = range(4)
 PALU_MODE_ROPE, PALU_MODE_ABSORBED = 0, 1
 PALU_KERNEL_TC_ROPE, PALU_KERNEL_TMA_ABSORBED, PALU_KERNEL_SIMT = 1, 2, 3
 PALU_FLAG_TEST_STALL = 0x80000000
+PALU_FLAG_ALIBI = 0x1
 
 DTYPES = {"f32": PALU_F32, "f16": PALU_F16, "bf16": PALU_BF16, "int4": PALU_INT4}
 MODES = {"rope": PALU_MODE_ROPE, "absorbed": PALU_MODE_ABSORBED}
@@ -262,30 +263,34 @@ def _require_contiguous(**tensors):
 
 
 def make_desc(*, n_heads, head_dim, group_size, rank_k, rank_v, latent_dtype, q_dtype, mode, rope_theta=10000.0,
-              max_batch=1, max_tokens=1, max_position=0, flags=0) -> palu_attn_desc:
+              max_batch=1, max_tokens=1, max_position=0, flags=0, v_dtype=None) -> palu_attn_desc:
+    """latent_dtype is the key latents' dtype and, unless v_dtype is given, the values' too
+    (v_dtype="int4" under fp16 / bf16 keys: int4 values only)."""
     k = DTYPES[latent_dtype]
+    v = DTYPES[v_dtype or latent_dtype]
     bk = PALU_F16 if k == PALU_INT4 else k
-    return palu_attn_desc(PALU_ABI_VERSION, n_heads, head_dim, group_size, rank_k, rank_v, k, k, bk,
+    return palu_attn_desc(PALU_ABI_VERSION, n_heads, head_dim, group_size, rank_k, rank_v, k, v, bk,
                           DTYPES[q_dtype], MODES[mode], float(rope_theta), max_batch, max_tokens, max_position, flags)
 
 
 class LatentCache:
     """Device latent cache in the layout palu_cache describes ([rows][capacity][n_g][r])."""
 
-    def __init__(self, rows, capacity, n_g, rank_k, rank_v, latent_dtype, device="cuda"):
+    def __init__(self, rows, capacity, n_g, rank_k, rank_v, latent_dtype, device="cuda", v_dtype=None):
         torch = _torch()
         self.rows, self.capacity, self.n_g = rows, capacity, n_g
         self.rank_k, self.rank_v, self.latent_dtype = rank_k, rank_v, latent_dtype
-        if latent_dtype == "int4":
-            self.hk = torch.zeros((rows, capacity, n_g, rank_k // 2), dtype=torch.uint8, device=device)
-            self.hv = torch.zeros((rows, capacity, n_g, rank_v // 2), dtype=torch.uint8, device=device)
-            self.k_scale = torch.zeros((rows, capacity, n_g), dtype=torch.float16, device=device)
-            self.v_scale = torch.zeros((rows, capacity, n_g), dtype=torch.float16, device=device)
-        else:
-            dt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[latent_dtype]
-            self.hk = torch.zeros((rows, capacity, n_g, rank_k), dtype=dt, device=device)
-            self.hv = torch.zeros((rows, capacity, n_g, rank_v), dtype=dt, device=device)
-            self.k_scale = self.v_scale = None
+        self.v_dtype = v_dtype or latent_dtype
+
+        def side(dtype, rank):
+            if dtype == "int4":
+                return (torch.zeros((rows, capacity, n_g, rank // 2), dtype=torch.uint8, device=device),
+                        torch.zeros((rows, capacity, n_g), dtype=torch.float16, device=device))
+            dt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[dtype]
+            return torch.zeros((rows, capacity, n_g, rank), dtype=dt, device=device), None
+
+        self.hk, self.k_scale = side(latent_dtype, rank_k)
+        self.hv, self.v_scale = side(self.v_dtype, rank_v)
 
     def c_struct(self) -> palu_cache:
         return palu_cache(_ptr(self.hk), _ptr(self.hv), _ptr(self.k_scale), _ptr(self.v_scale), self.capacity)
@@ -295,12 +300,12 @@ class PaluAttention:
     """Owns one handle and its torch-allocated workspace."""
 
     def __init__(self, bk, *, n_heads, head_dim, group_size, rank_k, rank_v, latent_dtype, q_dtype, mode,
-                 rope_theta=10000.0, max_batch=1, max_tokens=1, max_position=0, flags=0, stream=None):
+                 rope_theta=10000.0, max_batch=1, max_tokens=1, max_position=0, flags=0, v_dtype=None, stream=None):
         torch = _torch()
         self.desc = make_desc(n_heads=n_heads, head_dim=head_dim, group_size=group_size, rank_k=rank_k,
                               rank_v=rank_v, latent_dtype=latent_dtype, q_dtype=q_dtype, mode=mode,
                               rope_theta=rope_theta, max_batch=max_batch, max_tokens=max_tokens,
-                              max_position=max_position, flags=flags)
+                              max_position=max_position, flags=flags, v_dtype=v_dtype)
         st, nbytes = palu_attn_workspace_size(self.desc)
         check(st, "palu_attn_workspace_size")
         self.workspace = torch.empty(nbytes + 256, dtype=torch.uint8, device=bk.device)

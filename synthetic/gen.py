@@ -56,10 +56,15 @@ class Config:
     sigma_tau: float     # sigma_i = exp(-i / tau)
     hadamard: bool = False
     theta: float = 10000.0
+    v_dtype: str = ""    # value latents' dtype when it differs from the keys' ("int4": int4 values only)
 
     @property
     def n_groups(self) -> int:
         return self.n_heads // self.group_size
+
+    @property
+    def value_dtype(self) -> str:
+        return self.v_dtype or self.latent_dtype
 
     @property
     def bk_dtype(self) -> str:

@@ -28,10 +28,11 @@ class Case:
     """One workload on the GPU plus everything the oracle needs to check it."""
 
     def __init__(self, cfg: gen.Config, *, seq_lens=None, positions=None, q_pos=None, q_scale=1.0,
-                 capacity=None, max_position=0, fill="append", q_dtype=None):
+                 capacity=None, max_position=0, fill="append", q_dtype=None, alibi=False):
         import torch
         from rank_kv_cache_gb300 import palu as P
         self.cfg = cfg
+        self.alibi = alibi
         dev = torch.device("cuda:0")
         inp = gen.make_inputs(cfg, q_scale=q_scale)
         self.inp = inp
@@ -44,18 +45,21 @@ class Case:
         self.q_dtype = q_dtype or cfg.q_dtype
         self.q_t = gen.storage_round(inp["q"], self.q_dtype)
         self.bk_t = gen.storage_round(inp["bk"], cfg.bk_dtype)
+        vlat = cfg.value_dtype
         self.attn = P.PaluAttention(self.bk_t.to(dev), n_heads=cfg.n_heads, head_dim=cfg.head_dim,
                                     group_size=cfg.group_size, rank_k=cfg.rank, rank_v=cfg.rank, latent_dtype=lat,
                                     q_dtype=self.q_dtype, mode=cfg.mode, rope_theta=cfg.theta, max_batch=B,
-                                    max_tokens=self.capacity, max_position=max_position)
-        self.cache = P.LatentCache(B, self.capacity, cfg.n_groups, cfg.rank, cfg.rank, lat, device=dev)
-        if lat == "int4":
+                                    max_tokens=self.capacity, max_position=max_position, v_dtype=vlat,
+                                    flags=P.PALU_FLAG_ALIBI if alibi else 0)
+        self.cache = P.LatentCache(B, self.capacity, cfg.n_groups, cfg.rank, cfg.rank, lat, device=dev, v_dtype=vlat)
+        if "int4" in (lat, vlat):
+            # one source dtype for both sides: float32, rounded or quantised by the append kernel
             src_k = torch.from_numpy(np.ascontiguousarray(inp["hk"]))
             src_v = torch.from_numpy(np.ascontiguousarray(inp["hv"]))
         else:
             src_k = gen.storage_round(inp["hk"], lat)
             src_v = gen.storage_round(inp["hv"], lat)
-        if fill == "append" or lat == "int4":
+        if fill == "append" or "int4" in (lat, vlat):
             slot = torch.zeros(B, dtype=torch.int32, device=dev)
             self.attn.append(self.cache, src_k.to(dev), src_v.to(dev), slot)
         else:
@@ -67,18 +71,20 @@ class Case:
 
     def _oracle_latents(self):
         cfg, inp = self.cfg, self.inp
-        if cfg.latent_dtype == "int4":
-            ck, sk = O.quantize_int4(inp["hk"])
-            cv, sv = O.quantize_int4(inp["hv"])
-            self.ref_packed = (O.pack_int4(ck), sk, O.pack_int4(cv), sv)
-            # dequantised values are exact in float32 (pinned on the CPU); the oracle
-            # upcasts each slice it reads to float64
-            self.hk64 = O.dequant_int4(self.ref_packed[0], sk).astype(np.float32)
-            self.hv64 = O.dequant_int4(self.ref_packed[2], sv).astype(np.float32)
-        else:
+
+        def side(h, dtype):
+            if dtype == "int4":
+                codes, sc = O.quantize_int4(h)
+                # dequantised values are exact in float32 (pinned on the CPU); the oracle upcasts
+                # each slice it reads to float64
+                return O.pack_int4(codes), sc, O.dequant_int4(O.pack_int4(codes), sc).astype(np.float32)
             # fp16/bf16 values are exact in float32; the oracle upcasts to float64 per slice
-            self.hk64 = gen.storage_round(inp["hk"], cfg.latent_dtype).float().numpy()
-            self.hv64 = gen.storage_round(inp["hv"], cfg.latent_dtype).float().numpy()
+            return None, None, gen.storage_round(h, dtype).float().numpy()
+
+        pk, sk, self.hk64 = side(inp["hk"], cfg.latent_dtype)
+        pv, sv, self.hv64 = side(inp["hv"], cfg.value_dtype)
+        if cfg.latent_dtype == "int4":
+            self.ref_packed = (pk, sk, pv, sv)
         self.q64 = self.q_t.double().numpy()
         self.bk64 = self.bk_t.double().numpy()
 
@@ -103,7 +109,7 @@ class Case:
     def run_oracle(self, heads=None):
         cfg = self.cfg
         return O.decode(self.q64, self.hk64, self.hv64, self.bk64, self.seq_lens, cfg.group_size, mode=cfg.mode,
-                        theta=cfg.theta, positions=self.positions, q_pos=self.q_pos, heads=heads)
+                        theta=cfg.theta, positions=self.positions, q_pos=self.q_pos, heads=heads, alibi=self.alibi)
 
 
 def assert_close(out, ref, lse=None, lse_ref=None, *, f32=False, heads=None):

@@ -71,11 +71,35 @@ def test_bad_descriptor_rejected(field, value, status):
     assert st == status
 
 
-def test_only_the_test_stall_flag_is_accepted():
+def test_flags_accepted_per_mode():
     st, _ = P.palu_attn_workspace_size(_desc(flags=P.PALU_FLAG_TEST_STALL))
     assert st == P.PALU_OK
     st, _ = P.palu_attn_workspace_size(_desc(flags=P.PALU_FLAG_TEST_STALL | 2))
     assert st == P.PALU_ERR_INVALID_ARG
+    # ALiBi biases scores outside the keys: the absorbed path only
+    st, _ = P.palu_attn_workspace_size(_desc(mode="absorbed", flags=P.PALU_FLAG_ALIBI))
+    assert st == P.PALU_OK
+    st, _ = P.palu_attn_workspace_size(_desc(mode="rope", flags=P.PALU_FLAG_ALIBI))
+    assert st == P.PALU_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(latent_dtype="f16", v_dtype="int4"), P.PALU_OK),            # V-only int4
+    (dict(latent_dtype="bf16", v_dtype="int4"), P.PALU_OK),
+    (dict(latent_dtype="f16", v_dtype="int4", mode="absorbed"), P.PALU_OK),
+    (dict(latent_dtype="int4", v_dtype="f16"), P.PALU_ERR_UNSUPPORTED),
+    (dict(latent_dtype="f32", v_dtype="int4"), P.PALU_ERR_UNSUPPORTED),
+    (dict(group_size=1, rank_k=64, rank_v=64), P.PALU_OK),            # M-LRD
+    (dict(group_size=32), P.PALU_OK),                                 # J-LRD on the tensor-core path
+    (dict(group_size=16, latent_dtype="int4"), P.PALU_OK),
+    (dict(group_size=32, mode="absorbed"), P.PALU_ERR_UNSUPPORTED),
+    (dict(group_size=32, rank_k=128, rank_v=128), P.PALU_ERR_UNSUPPORTED),
+    (dict(group_size=32, latent_dtype="f32", q_dtype="f32"), P.PALU_ERR_UNSUPPORTED),
+    (dict(group_size=64, n_heads=64), P.PALU_ERR_UNSUPPORTED),
+])
+def test_granularity_and_value_dtype_variants(kw, status):
+    st, _ = P.palu_attn_workspace_size(_desc(**kw))
+    assert st == status
 
 
 def test_null_arguments_rejected_without_gpu():
