@@ -780,33 +780,45 @@ def bench_variant(args, dev, flush, peaks, peaks_src, base, over, flags):
     return e
 
 
-def run_next_rows(args, dev, flush, peaks, peaks_src):
-    """The steps next to the decode kernel, each timed with CUDA events (L2 flushed before each
-    launch) against its own roofline."""
+def next_row_table():
+    """name -> function(args, dev, flush, peaks, peaks_src) of every measurement next to the decode
+    workloads, in the order the bench line lists them."""
+    t = {}
+    for b in (1, 4):
+        t[f"llama2-7b-oproj-fp16-b{b}"] = (lambda b: lambda *a: bench_output_projection(*a, b))(b)
+    for name, base, over, flags in VARIANTS:
+        t[name] = (lambda base, over, flags: lambda *a: bench_variant(*a, base, over, flags))(base, over, flags)
+    t["llama2-7b-hybrid-int4-b4-t64k-s4-w64"] = lambda *a: bench_hybrid(*a)
+    for b, T, lat in ((1, 4096, "int4"), (4, 4096, "f16")):
+        t[f"llama2-7b-prefill-{lat}-b{b}-t4k"] = (lambda b, T, lat: lambda *a: bench_prefill(*a, b, T, lat))(b, T, lat)
+    return t
+
+
+def run_next_rows(args, dev, flush, peaks, peaks_src, only=None):
+    """The steps next to the decode kernel (output projection, granularity and storage variants,
+    hybrid cache, prefill producer), each timed with CUDA events (L2 flushed before each launch)
+    against its own roofline; `only` restricts the run to one of them."""
     import torch
     out = {}
-    for b in (1, 4):
-        name = f"llama2-7b-oproj-fp16-b{b}"
-        out[name] = bench_output_projection(args, dev, flush, peaks, peaks_src, b)
-        print(f"[bench] {name}: median {out[name]['kernel_us']['median']} us, frac {out[name]['roofline']['frac']}",
-              file=sys.stderr, flush=True)
-        torch.cuda.empty_cache()
-    for name, base, over, flags in VARIANTS:
-        out[name] = bench_variant(args, dev, flush, peaks, peaks_src, base, over, flags)
-        print(f"[bench] {name}: decode kernel median {out[name]['decode_kernel_us']['median']} us, "
-              f"{out[name]['roofline']['bound']} frac {out[name]['roofline']['frac']}", file=sys.stderr, flush=True)
-        torch.cuda.empty_cache()
-    out["llama2-7b-hybrid-int4-b4-t64k-s4-w64"] = bench_hybrid(args, dev, flush, peaks, peaks_src)
-    print(f"[bench] hybrid: call median {out['llama2-7b-hybrid-int4-b4-t64k-s4-w64']['call_us']['median']} us",
-          file=sys.stderr, flush=True)
-    torch.cuda.empty_cache()
-    for b, T, lat in ((1, 4096, "int4"), (4, 4096, "f16")):
-        name = f"llama2-7b-prefill-{lat}-b{b}-t4k"
-        out[name] = bench_prefill(args, dev, flush, peaks, peaks_src, b, T, lat)
-        print(f"[bench] {name}: median {out[name]['kernel_us']['median']} us, frac {out[name]['roofline']['frac']}",
+    for name, fn in next_row_table().items():
+        if only is not None and name != only:
+            continue
+        out[name] = e = fn(args, dev, flush, peaks, peaks_src)
+        t = e.get("kernel_us") or e.get("decode_kernel_us") or e.get("call_us")
+        print(f"[bench] {name}: median {t['median']} us, {e['roofline']['bound']} frac {e['roofline']['frac']}",
               file=sys.stderr, flush=True)
         torch.cuda.empty_cache()
     return out
+
+
+def run_one_next_row(args):
+    """--next-row NAME: that measurement alone, printed as one JSON line (profiling runs)."""
+    import torch
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    peaks, peaks_src = load_peaks()
+    return {"next_row": run_next_rows(args, dev, flush, peaks, peaks_src, only=args.next_row)}
 
 
 # ---------------------------------------------------------------------------
@@ -965,6 +977,7 @@ def main(argv=None):
     ap.add_argument("--per-config-cpu-seconds", type=float, default=3.0)
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch (profiling runs)")
     ap.add_argument("--tokens", type=int, default=None, help="override the workload's T (profiling runs)")
+    ap.add_argument("--next-row", default=None, help="run one next-row measurement alone (profiling runs)")
     ap.add_argument("--oracle-child", default=None, help=argparse.SUPPRESS)
     ap.add_argument("--oracle-child-cfg", default=None, help=argparse.SUPPRESS)
     args = ap.parse_args(argv)
@@ -973,6 +986,11 @@ def main(argv=None):
         return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.next_row is not None:
+        if args.next_row not in next_row_table():
+            ap.error(f"--next-row must be one of {sorted(next_row_table())}")
+        print(json.dumps(run_one_next_row(args)), flush=True)
+        return
     cfg = config_of(args.workload, args.batch, args.tokens)
     res = run_reference(args, cfg, args.workload) if args.impl == "reference" else run_gpu(args, cfg, args.workload)
     if res is not None:
