@@ -301,8 +301,9 @@ palu_status_t palu_output_proj(const void* W_fused, palu_dtype_t w_dtype, int64_
  * and a 64-token fp16 window around the compressed middle).
  *
  *   dense->k, dense->v  device [max_rows][capacity][n_heads][head_dim] in dense->dtype (F32, F16
- *                       or BF16). On the RoPE path the keys are stored rotated at their own
- *                       positions (as a dense KV cache holds them); on the absorbed path unrotated.
+ *                       or BF16), 8-byte aligned for F16 / BF16 and 4-byte for F32 (else
+ *                       PALU_ERR_INVALID_ARG). On the RoPE path the keys are stored rotated at their
+ *                       own positions (as a dense KV cache holds them); on the absorbed path unrotated.
  *   dense->n_tokens     device [batch] int32: tokens 0 .. n_tokens[b] - 1 of row b are attended
  *                       (their order does not matter); a count outside [0, capacity] is clamped
  *                       and recorded in the error word.

@@ -9,8 +9,9 @@
 // The latent middle is decoded by the regular decode kernels (its output o_mid normalised by its
 // own softmax, and its natural-log lse). merge_dense_kernel then takes one CTA per (batch row,
 // head): it rotates the query at q_pos (RoPE path; the dense keys are stored rotated at their own
-// positions), scores the row's dense tokens (8 warps, one token per warp at a time, each lane
-// holding d_h / 32 dimensions, scores reduced across the warp), runs an online softmax per warp
+// positions), scores the row's dense tokens (8 warps, each loading four of its tokens at a time
+// before scoring them; each lane holds d_h / 32 dimensions, scores reduced across the warp), runs an
+// online softmax per warp
 // with the p v accumulation, merges the warps, and finally merges the dense segment with the
 // middle:
 //   lse = ln(e^lse_mid + sum_dense e^s),   out *= e^(lse_mid - lse),   out_dense = sum p v / e^lse
@@ -24,7 +25,29 @@ constexpr int kHThreads = 256;
 constexpr int kHWarps = kHThreads / 32;
 constexpr int kHMaxDh = 128;
 
-__device__ __forceinline__ float load_elem(const void* p, int dtype, int64_t i) { return load_as_f32(p, dtype, i); }
+constexpr int kHAhead = 4;   // tokens each warp loads before scoring them
+
+// `per` (<= 4) consecutive elements at index i as floats; one 8-byte load for four 16-bit values
+__device__ __forceinline__ void load_row_part(const void* p, int dtype, int64_t i, int per, float (&x)[4]) {
+  if (per == 4 && dtype != kF32) {
+    const uint2 u = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p) + i);
+    const uint32_t w[2] = {u.x, u.y};
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      if (dtype == kF16) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
+        x[2 * j] = f.x;
+        x[2 * j + 1] = f.y;
+      } else {
+        x[2 * j] = __uint_as_float(w[j] << 16);
+        x[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+      }
+    }
+    return;
+  }
+#pragma unroll
+  for (int e = 0; e < 4; ++e) x[e] = e < per ? load_as_f32(p, dtype, i + e) : 0.f;
+}
 
 __global__ void __launch_bounds__(kHThreads) merge_dense_kernel(DenseArgs d) {
   __shared__ float qs[kHMaxDh];
@@ -65,25 +88,31 @@ __global__ void __launch_bounds__(kHThreads) merge_dense_kernel(DenseArgs d) {
 
   // online softmax of this warp's tokens (base 2)
   float m = -INFINITY, l = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int t = warp; t < D; t += kHWarps) {
-    const int64_t row = (((int64_t)b * d.capacity + t) * d.n_heads + i) * dh + lane * per;
-    float kv[4], vv[4];
+  // warp w takes tokens w, w + 8, ...; each round loads kHAhead tokens' rows before scoring them
+  for (int t0 = warp; t0 < D; t0 += kHWarps * kHAhead) {
+    float kv[kHAhead][4], vv[kHAhead][4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      kv[e] = e < per ? load_elem(d.k, d.dtype, row + e) : 0.f;
-      vv[e] = e < per ? load_elem(d.v, d.dtype, row + e) : 0.f;
+    for (int a = 0; a < kHAhead; ++a) {
+      const int t = t0 + a * kHWarps;
+      const int64_t row = (((int64_t)b * d.capacity + (t < D ? t : 0)) * d.n_heads + i) * dh + lane * per;
+      load_row_part(d.k, d.dtype, row, per, kv[a]);
+      load_row_part(d.v, d.dtype, row, per, vv[a]);
     }
-    float s = 0.f;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) s = fmaf(qv[e], kv[e], s);
-    s = warp_sum(s);
-    const float mn = fmaxf(m, s);
-    const float al = m == -INFINITY ? 0.f : exp2f(m - mn);
-    const float p = exp2f(s - mn);
-    l = l * al + p;
+    for (int a = 0; a < kHAhead; ++a) {
+      if (t0 + a * kHWarps >= D) break;   // warp-uniform
+      float s = 0.f;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) acc[e] = acc[e] * al + p * vv[e];
-    m = mn;
+      for (int e = 0; e < 4; ++e) s = fmaf(qv[e], kv[a][e], s);
+      s = warp_sum(s);
+      const float mn = fmaxf(m, s);
+      const float al = m == -INFINITY ? 0.f : exp2f(m - mn);
+      const float p = exp2f(s - mn);
+      l = l * al + p;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[e] = acc[e] * al + p * vv[a][e];
+      m = mn;
+    }
   }
   if (lane == 0) {
     wm[warp] = m;

@@ -515,8 +515,9 @@ palu_status_t palu_decode_hybrid(palu_attn_t h, const void* q, const palu_cache*
   if (!dense->k || !dense->v || !dense->n_tokens || dense->capacity <= 0 || dense->capacity > (int64_t(1) << 31) ||
       (unsigned)dense->dtype > PALU_BF16)
     return PALU_ERR_INVALID_ARG;
-  const size_t es = dense->dtype == PALU_F32 ? 4 : 2;
-  if ((uintptr_t)dense->k % es || (uintptr_t)dense->v % es) return PALU_ERR_INVALID_ARG;
+  // 16-bit rows are read four elements (8 bytes) at a time
+  const size_t al = dense->dtype == PALU_F32 ? 4 : 8;
+  if ((uintptr_t)dense->k % al || (uintptr_t)dense->v % al) return PALU_ERR_INVALID_ARG;
   // the latent middle: out and lse hold its own softmax until the merge below
   palu_status_t st = palu_decode_attn(h, q, cache, seq_lens, positions, q_pos, batch, max_seq_len, out, lse, stream);
   if (st != PALU_OK) return st;
