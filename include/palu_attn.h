@@ -92,7 +92,11 @@ typedef struct palu_attn_desc {
   int head_dim;           /* d_h: 64 or 128 */
   int group_size;         /* s: 1, 2, 4 or 8 (M-LRD is s = 1); 16 or 32 (up to J-LRD, s = n) on the
                              RoPE path with head_dim 128, ranks 256 and F16/BF16/INT4 latents
-                             ("方法细节", M-LRD / G-LRD / J-LRD paragraphs); n_heads % s == 0 */
+                             ("方法细节", M-LRD / G-LRD / J-LRD paragraphs); n_heads % s == 0.
+                             s = 1 or 2 with ranks 64 s, head_dim 128, F16/BF16 latents and
+                             n_heads % 4 == 0 run packed four heads at a time with a block-diagonal
+                             B_k (the workspace then holds 4 / s times the B_k bytes); the output
+                             layout is unchanged ([batch][n_heads][rank_v]) */
   int rank_k;             /* r_k per group: 64, 128 or 256 */
   int rank_v;             /* r_v per group: 64, 128 or 256 */
   palu_dtype_t k_dtype;   /* key-latent storage */

@@ -48,8 +48,13 @@ struct DecodeArgs {
   // an atomic that it resets afterwards) merges that unit's partials into out / lse, and no
   // merge kernel is launched. counters: [max_batch][n_heads], zero between calls.
   unsigned* counters;
-  float* out;
+  float* out;                 // [B][n][out_rv ? out_rv : rv]
   float* lse;
+  // Packed groups (out_rv > 0): the kernels run groups of four heads whose rv = 256 latent
+  // columns hold 4 / pack_s source groups of out_rv ranks each; head h's output is the slice of
+  // its own source group, columns ((h % 4) / pack_s) * out_rv + [0, out_rv).
+  int out_rv;
+  int pack_s;
   // failure-detection test hook (PALU_FLAG_TEST_STALL): the tensor-core kernel's H_v
   // producer issues nothing; wait_ns bounds every mbarrier wait of that kernel
   int test_stall;
@@ -61,7 +66,7 @@ struct DecodeArgs {
 // create-time set-up
 cudaError_t launch_rope_table(float2* tab, uint64_t* phase, int64_t max_pos, int dh, double theta, cudaStream_t st);
 cudaError_t launch_copy_bk(const void* src, int bk_dtype, void* dst, void* dst_t, int mma_dtype, int n_g,
-                           int rk, int cols, int dh, int perm8, cudaStream_t st);
+                           int rk, int cols, int dh, int perm8, int pack, int src_s, int src_rk, cudaStream_t st);
 
 // per-call kernels
 cudaError_t launch_qprep(int mode, const void* q, int q_dtype, const DecodeArgs& a, const int32_t* q_pos,

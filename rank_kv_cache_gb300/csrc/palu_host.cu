@@ -55,10 +55,36 @@ palu_status_t check_desc(const palu_attn_desc* d) {
   return PALU_OK;
 }
 
+// The group shape the decode kernels run. G-LRD groups of s = 1 (M-LRD) or s = 2 heads with
+// r = 64 s ranks each, fp16 or bf16 latents and d_h = 128, are run as groups of four heads and
+// 256 ranks: 4 / s neighbouring groups' cache rows are contiguous, so the cache is read as is, and
+// their B_k blocks form a block-diagonal B_k of the packed group (zeros elsewhere). A head's
+// scores then equal its own group's exactly (the other groups' latents meet zeros); its output
+// is the slice of the packed group's 256 latent columns that holds its own group's ranks, which
+// the split merge writes. This puts those shapes on the tensor-core and TMA-streamed kernels.
+struct KShape {
+  int s, rk, rv, pack;   // pack = source groups per kernel group (1: none)
+  int64_t n_g;
+};
+
+KShape kernel_shape(const palu_attn_desc& d) {
+  KShape k{d.group_size, d.rank_k, d.rank_v, 1, d.n_heads / d.group_size};
+  if ((d.group_size == 1 || d.group_size == 2) && d.head_dim == 128 && d.rank_k == 64 * d.group_size &&
+      d.rank_v == d.rank_k && d.n_heads % 4 == 0 && d.k_dtype == d.v_dtype &&
+      (d.k_dtype == PALU_F16 || d.k_dtype == PALU_BF16)) {
+    k.pack = 4 / d.group_size;
+    k.s = 4;
+    k.rk = k.rv = 256;
+    k.n_g = d.n_heads / 4;
+  }
+  return k;
+}
+
 WsLayout layout_of(const palu_attn_desc& d) {
   WsLayout L{};
-  const int64_t n_g = d.n_heads / d.group_size;
-  const int64_t cols = (int64_t)d.group_size * d.head_dim;
+  const KShape k = kernel_shape(d);
+  const int64_t n_g = k.n_g;
+  const int64_t cols = (int64_t)k.s * d.head_dim;
   L.max_pos = d.max_position > 0 ? d.max_position : d.max_tokens;
   int64_t ms = (d.max_tokens + kSimtTile - 1) / kSimtTile;
   L.max_splits = int(ms < 1 ? 1 : (ms > 256 ? 256 : ms));
@@ -66,18 +92,18 @@ WsLayout layout_of(const palu_attn_desc& d) {
   L.err = off;
   off = align256(off + 256);
   L.bk = off;
-  off = align256(off + (size_t)n_g * d.rank_k * cols * elem_bytes(d.bk_dtype));
+  off = align256(off + (size_t)n_g * k.rk * cols * elem_bytes(d.bk_dtype));
   L.bkt = off;
-  if (d.mode == PALU_MODE_ROPE && d.k_dtype != PALU_F32) off = align256(off + (size_t)n_g * cols * d.rank_k * 2);
+  if (d.mode == PALU_MODE_ROPE && d.k_dtype != PALU_F32) off = align256(off + (size_t)n_g * cols * k.rk * 2);
   L.rope = off;
   if (d.mode == PALU_MODE_ROPE) off = align256(off + (size_t)L.max_pos * (d.head_dim / 2) * sizeof(float2));
   L.phase = off;
   if (d.mode == PALU_MODE_ROPE) off = align256(off + (size_t)(d.head_dim / 2) * sizeof(uint64_t));
-  const int qw = d.mode == PALU_MODE_ROPE ? d.head_dim : d.rank_k;
+  const int qw = d.mode == PALU_MODE_ROPE ? d.head_dim : k.rk;
   L.qbuf = off;
   off = align256(off + (size_t)d.max_batch * d.n_heads * qw * sizeof(float));
   L.part_o = off;
-  off = align256(off + (size_t)d.max_batch * d.n_heads * L.max_splits * d.rank_v * sizeof(float));
+  off = align256(off + (size_t)d.max_batch * d.n_heads * L.max_splits * k.rv * sizeof(float));
   L.part_ml = off;
   off = align256(off + (size_t)d.max_batch * d.n_heads * L.max_splits * sizeof(float2));
   L.counters = off;
@@ -130,7 +156,8 @@ struct palu_attn {
   char* ws;
   size_t ws_bytes;
   WsLayout L;
-  int n_g;
+  int n_g;       // groups of the descriptor (cache rows, append, latent production)
+  KShape ks;     // the group shape the decode kernels run
   int device;
   int sm_count;
   int mma_dtype;
@@ -186,6 +213,7 @@ palu_status_t palu_attn_create(const palu_attn_desc* desc, const void* B_k, void
   h->ws_bytes = workspace_bytes;
   h->L = L;
   h->n_g = desc->n_heads / desc->group_size;
+  h->ks = kernel_shape(*desc);
   h->device = attr.device;
   h->sm_count = sms;
   h->mma_dtype = desc->k_dtype == PALU_BF16 ? kBF16 : kF16;
@@ -194,11 +222,12 @@ palu_status_t palu_attn_create(const palu_attn_desc* desc, const void* B_k, void
   cudaError_t e = cudaMemsetAsync(h->ws + L.err, 0, 256, s);
   if (e == cudaSuccess)
     e = cudaMemsetAsync(h->ws + L.counters, 0, (size_t)desc->max_batch * desc->n_heads * sizeof(unsigned), s);
-  const int cols = desc->group_size * desc->head_dim;
+  const KShape& k = h->ks;
   void* bkt = (desc->mode == PALU_MODE_ROPE && desc->k_dtype != PALU_F32) ? h->ws + L.bkt : nullptr;
   if (e == cudaSuccess)
-    e = launch_copy_bk(B_k, to_dt(desc->bk_dtype), h->ws + L.bk, bkt, h->mma_dtype, h->n_g, desc->rank_k, cols,
-                       desc->head_dim, desc->k_dtype == PALU_INT4 ? 1 : 0, s);
+    e = launch_copy_bk(B_k, to_dt(desc->bk_dtype), h->ws + L.bk, bkt, h->mma_dtype, (int)k.n_g, k.rk,
+                       k.s * desc->head_dim, desc->head_dim, desc->k_dtype == PALU_INT4 ? 1 : 0, k.pack,
+                       desc->group_size, desc->rank_k, s);
   if (e == cudaSuccess && desc->mode == PALU_MODE_ROPE)
     e = launch_rope_table(reinterpret_cast<float2*>(h->ws + L.rope), reinterpret_cast<uint64_t*>(h->ws + L.phase),
                           L.max_pos, desc->head_dim, desc->rope_theta, s);
@@ -398,11 +427,13 @@ static void fill_args(const palu_attn* h, const palu_cache* cache, int batch, in
   a.v_scale = static_cast<const __half*>(cache->v_scale);
   a.capacity = cache->capacity;
   a.n_heads = d.n_heads;
-  a.n_g = h->n_g;
-  a.s = d.group_size;
+  a.n_g = (int)h->ks.n_g;
+  a.s = h->ks.s;
   a.dh = d.head_dim;
-  a.rk = d.rank_k;
-  a.rv = d.rank_v;
+  a.rk = h->ks.rk;
+  a.rv = h->ks.rv;
+  a.out_rv = h->ks.pack > 1 ? d.rank_v : 0;   // packed groups: the merge writes each head's own slice
+  a.pack_s = d.group_size;
   a.k_dtype = to_dt(d.k_dtype);
   a.v_dtype = to_dt(d.v_dtype);
   a.bk_dtype = to_dt(d.bk_dtype);
@@ -437,7 +468,7 @@ static int plan_decode(const palu_attn* h, DecodeArgs& a) {
                    : kernel == PALU_KERNEL_TMA_ABSORBED ? abs_stage_tokens()
                                                         : kSimtTile;
   const int64_t tiles = a.max_seq_len > 0 ? (a.max_seq_len + tile - 1) / tile : 1;
-  const int64_t units = (int64_t)a.batch * h->n_g * (kernel == PALU_KERNEL_TC_ROPE ? tc_ctas_per_group(a) : 1);
+  const int64_t units = (int64_t)a.batch * a.n_g * (kernel == PALU_KERNEL_TC_ROPE ? tc_ctas_per_group(a) : 1);
   // CTA fixed costs in tiles, as measured on GB300 at the 32K-64K workloads: about four
   // 128-token tiles for the tensor-core kernel, eight 64-token stages for the absorbed stream
   const int fixed = kernel == PALU_KERNEL_TC_ROPE ? 4 : kernel == PALU_KERNEL_TMA_ABSORBED ? 8 : 1;

@@ -48,19 +48,30 @@ cudaError_t launch_rope_table(float2* tab, uint64_t* phase, int64_t max_pos, int
 // perm8 (int4 caches): within each group of eight ranks, position p holds rank [0,2,4,6,1,3,5,7][p],
 // the order in which the int4 converter emits a packed word's codes; permuting K in both MMA
 // operands alike leaves the product unchanged.
+// pack > 1 (packed groups, 16-bit B_k only): the n_g x rk x cols copy is the block-diagonal B_k of
+// kernel groups made of `pack` source groups of src_s heads and src_rk ranks: source group jg of
+// kernel group g fills ranks [jg src_rk, (jg + 1) src_rk) x its own heads' columns, zeros elsewhere.
 __global__ void copy_bk_kernel(const void* src, int bk_dtype, void* dst, void* dst_t, int mma_dtype, int n_g,
-                               int rk, int cols, int dh, int perm8) {
+                               int rk, int cols, int dh, int perm8, int pack, int src_s, int src_rk) {
   const int64_t n = (int64_t)n_g * rk * cols;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
     const int c = int(i % cols);
     const int m = int((i / cols) % rk);
     const int g = int(i / ((int64_t)cols * rk));
     const int esz = bk_dtype == kF32 ? 4 : 2;
+    // the source element: the same index, or for packed groups the block-diagonal expansion
+    int64_t si = i;
+    if (pack > 1) {
+      const int jg = (c / dh) / src_s;   // source group of this column within the kernel group
+      si = (m / src_rk == jg) ? (((int64_t)g * pack + jg) * src_rk + (m - jg * src_rk)) * ((int64_t)src_s * dh) +
+                                    (c - jg * src_s * dh)
+                              : -1;
+    }
     // plain byte copy of the original layout
-    if (esz == 4) static_cast<float*>(dst)[i] = static_cast<const float*>(src)[i];
-    else static_cast<uint16_t*>(dst)[i] = static_cast<const uint16_t*>(src)[i];
+    if (esz == 4) static_cast<float*>(dst)[i] = si >= 0 ? static_cast<const float*>(src)[si] : 0.f;
+    else static_cast<uint16_t*>(dst)[i] = si >= 0 ? static_cast<const uint16_t*>(src)[si] : uint16_t(0);
     if (dst_t) {
-      const float v = load_as_f32(src, bk_dtype, i);
+      const float v = si >= 0 ? load_as_f32(src, bk_dtype, si) : 0.f;
       const int j = c / dh, d = c % dh;
       const int ct = ((cols / dh) % 2 == 0) ? (j / 2) * 2 * dh + 2 * d + (j & 1) : c;
       const int mt = perm8 ? (m & ~7) | ((m & 1) << 2) | ((m & 7) >> 1) : m;
@@ -72,10 +83,11 @@ __global__ void copy_bk_kernel(const void* src, int bk_dtype, void* dst, void* d
 }
 
 cudaError_t launch_copy_bk(const void* src, int bk_dtype, void* dst, void* dst_t, int mma_dtype, int n_g, int rk,
-                           int cols, int dh, int perm8, cudaStream_t st) {
+                           int cols, int dh, int perm8, int pack, int src_s, int src_rk, cudaStream_t st) {
   const int64_t n = (int64_t)n_g * rk * cols;
   const int blocks = int((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
-  copy_bk_kernel<<<blocks, 256, 0, st>>>(src, bk_dtype, dst, dst_t, mma_dtype, n_g, rk, cols, dh, perm8);
+  copy_bk_kernel<<<blocks, 256, 0, st>>>(src, bk_dtype, dst, dst_t, mma_dtype, n_g, rk, cols, dh, perm8, pack, src_s,
+                                         src_rk);
   return cudaGetLastError();
 }
 

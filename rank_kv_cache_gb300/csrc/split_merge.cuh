@@ -36,10 +36,13 @@ __device__ __forceinline__ void merge_partials(const DecodeArgs& a, int b, int h
     }
   }
   __syncthreads();
-  for (int idx = tid; idx < nh * a.rv; idx += nthreads) {
-    const int j = idx / a.rv, c = idx % a.rv;
+  // packed groups: head h's output is its own source group's out_rv columns of the rv computed
+  const int orv = a.out_rv > 0 ? a.out_rv : a.rv;
+  for (int idx = tid; idx < nh * orv; idx += nthreads) {
+    const int j = idx / orv, c = idx % orv;
     const int64_t bh = (int64_t)b * a.n_heads + h0 + j;
-    const float* po = a.part_o + bh * ns * a.rv + c;
+    const int c0 = a.out_rv > 0 ? (((h0 + j) & 3) / a.pack_s) * orv : 0;
+    const float* po = a.part_o + bh * ns * a.rv + c0 + c;
     const float* wj = w + j * ns;
     float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
     int k = 0;
@@ -54,7 +57,7 @@ __device__ __forceinline__ void merge_partials(const DecodeArgs& a, int b, int h
     for (; k < ns; ++k) o0 = fmaf(__ldcg(po + (int64_t)k * a.rv), wj[k], o0);
     const float o = (o0 + o1) + (o2 + o3);
     const float L = ML[2 * j + 1];
-    a.out[bh * a.rv + c] = L > 0.f ? o / L : 0.f;
+    a.out[bh * orv + c] = L > 0.f ? o / L : 0.f;
     if (a.lse && c == 0) a.lse[bh] = L > 0.f ? (ML[2 * j] + log2f(L)) * 0.69314718055994531f : -INFINITY;
   }
 }

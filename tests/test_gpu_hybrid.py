@@ -72,6 +72,12 @@ def test_rope_fp16_middle_with_sinks_and_window(T):
     _check(_run(cfg, [T, max(1, T // 2)], [SINKS + WINDOW, SINKS + 10]))
 
 
+def test_rope_m_lrd_middle_packed_groups():
+    # s = 1 rank 64 runs as packed groups; the dense merge rescales each head's own latent slice
+    cfg = gen.ROPE_FP16.with_(T=300, batch=2, group_size=1, rank=64)
+    _check(_run(cfg, [300, 130], [SINKS + WINDOW, SINKS + 3], seed=3))
+
+
 def test_rope_int4_middle_bf16_dense():
     cfg = gen.ROPE_INT4.with_(T=500, batch=2)
     _check(_run(cfg, [500, 300], [SINKS + WINDOW, SINKS + WINDOW], "bf16", seed=1))

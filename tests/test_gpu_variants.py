@@ -67,10 +67,36 @@ def test_group_sizes_on_the_tensor_core_kernel(s):
     _check(c)
 
 
-def test_per_head_decomposition_m_lrd():
-    # s = 1, rank 64 per head: the same total rank as G-LRD with s = 4 and rank 256
-    cfg = gen.ROPE_FP16.with_(T=300, batch=2, group_size=1, rank=64)
-    _check(Case(cfg, seq_lens=[300, 150]))
+# M-LRD (s = 1, rank 64 per head: the same total rank as G-LRD with s = 4 and rank 256) and G-LRD
+# with s = 2 and rank 128 run as packed groups of four heads with a block-diagonal B_k on the
+# tensor-core and TMA-stream kernels; every head's output is its own group's latent slice
+@pytest.mark.parametrize("mode,lat,s,T,batch,seqs,qs", [
+    ("rope", "f16", 1, 300, 2, [300, 150], 1.0),
+    ("rope", "bf16", 1, 129, 2, [129, 128], 8.0),
+    ("rope", "f16", 2, 1000, 2, [1000, 257], 1.0),
+    ("rope", "f16", 1, 100, 1, [100], 1.0),          # fewer than 128 cache rows: CUDA-core kernel
+    ("absorbed", "f16", 1, 333, 2, [333, 65], 1.0),
+    ("absorbed", "bf16", 2, 200, 2, [200, 129], 8.0),
+])
+def test_packed_groups_m_lrd_and_s2(mode, lat, s, T, batch, seqs, qs):
+    from rank_kv_cache_gb300 import palu as P
+    base = gen.ROPE_FP16 if mode == "rope" else gen.ABSORBED_FP16
+    cfg = base.with_(T=T, batch=batch, group_size=s, rank=64 * s, latent_dtype=lat)
+    c = Case(cfg, seq_lens=seqs, q_scale=qs)
+    fast = P.PALU_KERNEL_TC_ROPE if mode == "rope" else P.PALU_KERNEL_TMA_ABSORBED
+    assert _kernel(c) == (fast if batch * T >= 128 else P.PALU_KERNEL_SIMT)
+    _check(c)
+
+
+def test_packed_m_lrd_long_sampled_heads():
+    from rank_kv_cache_gb300 import palu as P
+    cfg = gen.ROPE_FP16.with_(T=4096, batch=1, group_size=1, rank=64)
+    c = Case(cfg)
+    assert _kernel(c) == P.PALU_KERNEL_TC_ROPE
+    out, lse = c.run_gpu()
+    heads = [(0, 0), (0, 1), (0, 2), (0, 3), (0, 30)]
+    ref, lse_ref = c.run_oracle(heads=heads)
+    assert_close(out, ref, lse, lse_ref, heads=heads)
 
 
 def test_joint_decomposition_j_lrd():
