@@ -33,6 +33,9 @@ design notes):
     element 2j in the low nibble, 2j+1 in the high nibble (two's complement);
   * an empty sequence yields o = 0 and lse = -inf.
 
+The per-page factorised decode follows [Puzzle] section 3.3 (decode_paged, factor_page and
+factor_page_gram); its readings are given in its docstring.
+
 Every function below is pinned by a CPU test against something other than
 itself (closed forms, the pages' worked numbers, library routines, brute force,
 the identities the pages derive); none is "parity unpinned".
@@ -286,6 +289,84 @@ def mha_decode(q, x, wk, wv, seq_lens, *, theta: float = 10000.0, rope: bool = T
                 sc = sc + alibi_bias(alibi_slopes(n)[i], pos, qp)
             a[b, i], lse[b, i] = softmax_attend(sc, V)
     return a, lse
+
+
+def factor_page(x: np.ndarray, r: int):
+    """One page's rank-r factors ([Puzzle] section 3.3, eq. 2): the truncated SVD X ~= L R of a
+    P x d page with L = U_r (P x r) and R = S_r W_r^T (r x d)."""
+    u, s, wt = np.linalg.svd(np.asarray(x, np.float64), full_matrices=False)
+    return u[:, :r], s[:r, None] * wt[:r]
+
+
+def factor_page_gram(x: np.ndarray, r: int):
+    """The same factors the way [Puzzle] section 3.3 obtains them for short, wide pages: the top-r
+    eigenvectors Q_r of the P x P Gram matrix G = X X^T give L = Q_r and R = Q_r^T X."""
+    x = np.asarray(x, np.float64)
+    w, q = np.linalg.eigh(x @ x.T)
+    qr = q[:, np.argsort(w)[::-1][:r]]
+    return qr, qr.T @ x
+
+
+def decode_paged(q, lk, rk, lv, rv, n_pages, dense_k, dense_v, n_dense, *, mode: str = "rope",
+                 theta: float = 10000.0, q_pos=None, heads=None):
+    """Decode over a page-factorised cache next to dense sink and window tokens ([Puzzle] section
+    3.3, step 4: every completed page p of a head holds K_p ~= L_p^K R_p^K and V_p ~= L_p^V R_p^V;
+    the page's scores are s_p = (q R_p^K^T) L_p^K^T / sqrt(d) and its values are read as
+    L_p^V R_p^V without rebuilding the page; dense and factorised pages share one softmax).
+
+    Readings: the factorised pages hold the keys as the cache holds them, i.e. already rotated on
+    the RoPE path, so they are scored like the dense tokens against q rotated at q_pos (no
+    rotation on the absorbed path); the value read is the plain product p (L^V R^V). The output is
+    split like decode_hybrid's: the factorised pages' part and the dense tokens' part, both
+    normalised by the shared denominator (their sum is the attention output).
+
+    lk [B][Pmax][n][P][r_k], rk [B][Pmax][n][r_k][d_h], lv [B][Pmax][n][P][r_v],
+    rv [B][Pmax][n][r_v][d_h]; n_pages [B]; dense_k, dense_v [B][D][n][d_h]; n_dense [B].
+    Returns (o_pages [B][n][d_h], o_dense [B][n][d_h], lse [B][n]); rows not in ``heads`` are NaN.
+    """
+    B, n, d_h = q.shape
+    o_pg = np.full((B, n, d_h), np.nan)
+    o_den = np.full((B, n, d_h), np.nan)
+    lse = np.full((B, n), np.nan)
+    todo = heads if heads is not None else [(b, i) for b in range(B) for i in range(n)]
+    for b, i in todo:
+        npg = int(n_pages[b])
+        D = int(n_dense[b])
+        qi = np.asarray(q[b, i], np.float64)
+        if mode == "rope":
+            if q_pos is None:
+                raise ValueError("the RoPE path needs q_pos")
+            q_use = rope_rotate(qi, float(q_pos[b]), theta)
+        elif mode == "absorbed":
+            q_use = qi
+        else:
+            raise ValueError(mode)
+        s_pages = []
+        for p in range(npg):
+            u = np.asarray(rk[b, p, i], np.float64) @ q_use              # q R^T: one value per rank
+            s_pages.append((np.asarray(lk[b, p, i], np.float64) @ u) / math.sqrt(d_h))
+        s_pg = np.concatenate(s_pages) if s_pages else np.zeros(0)
+        kd = np.asarray(dense_k[b, :D, i, :], np.float64)
+        s_den = (kd @ q_use) / math.sqrt(d_h) if D else np.zeros(0)
+        s_all = np.concatenate([s_pg, s_den])
+        if s_all.size == 0:
+            o_pg[b, i], o_den[b, i], lse[b, i] = 0.0, 0.0, -math.inf
+            continue
+        m = s_all.max()
+        e = np.exp(s_all - m)
+        l = e.sum()
+        prob = e / l
+        acc = np.zeros(d_h)
+        off = 0
+        for p in range(npg):
+            P = lk.shape[3]
+            w = prob[off:off + P] @ np.asarray(lv[b, p, i], np.float64)   # p L^V: one value per rank
+            acc += w @ np.asarray(rv[b, p, i], np.float64)
+            off += P
+        o_pg[b, i] = acc
+        o_den[b, i] = prob[off:] @ np.asarray(dense_v[b, :D, i, :], np.float64) if D else 0.0
+        lse[b, i] = m + math.log(l)
+    return o_pg, o_den, lse
 
 
 # ---------------------------------------------------------------------------

@@ -2,7 +2,7 @@
 
 Every mutation below is a realistic slip: wrong rotation sign, wrong pairing,
 wrong frequency schedule, wrong head-to-group map, wrong score scale, wrong
-rounding mode, swapped nibbles. The pin tests must fail on each one.
+rounding mode, swapped nibbles, the wrong factor of a page. The pin tests must fail on each one.
 """
 import math
 
@@ -144,6 +144,20 @@ def _alibi_bias_wrong_sign(slope, pos, qp):
     return slope * (float(qp) - np.asarray(pos, np.float64))
 
 
+_decode_paged = O.decode_paged
+
+
+def _decode_paged_values_from_key_factors(q, lk, rk, lv, rv, *a, **kw):
+    # reads every page's values through its key factors
+    return _decode_paged(q, lk, rk, lk, rk, *a, **kw)
+
+
+def _factor_page_without_singular_values(x, r):
+    # R = W_r^T: the singular values dropped from the right factor
+    u, s, wt = np.linalg.svd(np.asarray(x, np.float64), full_matrices=False)
+    return u[:, :r], wt[:r]
+
+
 ALL_PINS = [getattr(P, n) for n in dir(P) if n.startswith("test_")]
 
 MUTATIONS = {
@@ -162,6 +176,8 @@ MUTATIONS = {
     "latents_first_group_only": ("project_latents", _project_latents_first_group),
     "hybrid_segments_normalised_apart": ("decode_hybrid", _decode_hybrid_separate_softmax),
     "alibi_bias_wrong_sign": ("alibi_bias", _alibi_bias_wrong_sign),
+    "paged_values_from_key_factors": ("decode_paged", _decode_paged_values_from_key_factors),
+    "page_factor_without_singular_values": ("factor_page", _factor_page_without_singular_values),
 }
 
 

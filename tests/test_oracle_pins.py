@@ -515,6 +515,123 @@ def test_hybrid_with_an_empty_middle_is_dense_softmax_attention():
 
 
 # ---------------------------------------------------------------------------
+# Page-factorised cache ([Puzzle] section 3.3)
+# ---------------------------------------------------------------------------
+
+def test_page_factors_are_the_truncated_svd_and_match_the_gram_route():
+    rng = np.random.default_rng(61)
+    x = rng.standard_normal((8, 20)) * np.exp(-np.arange(20) / 6.0)[None, :]
+    sv = np.linalg.svd(x, compute_uv=False)
+    for r in (1, 3, 8):
+        L, R = O.factor_page(x, r)
+        Lg, Rg = O.factor_page_gram(x, r)
+        # L has orthonormal columns, and the product is the same rank-r approximation both ways
+        np.testing.assert_allclose(L.T @ L, np.eye(r), atol=1e-13)
+        np.testing.assert_allclose(Lg.T @ Lg, np.eye(r), atol=1e-12)
+        np.testing.assert_allclose(L @ R, Lg @ Rg, atol=1e-11)
+        # Eckart-Young: the residual is the discarded singular values
+        assert abs(np.sum((x - L @ R) ** 2) - np.sum(sv[r:] ** 2)) < 1e-10
+    L, R = O.factor_page(x, 8)                      # full page rank: exact
+    np.testing.assert_allclose(L @ R, x, atol=1e-12)
+
+
+def _pages_of(keys, vals, P, r):
+    """Factorise [T][n][d] keys and values page by page (T a multiple of P): [n_pages][n][...] factors."""
+    T, n, _ = keys.shape
+    lk, rk, lv, rv = [], [], [], []
+    for p in range(T // P):
+        f = [O.factor_page(keys[p * P:(p + 1) * P, i], r) for i in range(n)]
+        g = [O.factor_page(vals[p * P:(p + 1) * P, i], r) for i in range(n)]
+        lk.append([a for a, _ in f]); rk.append([b for _, b in f])
+        lv.append([a for a, _ in g]); rv.append([b for _, b in g])
+    return np.array(lk), np.array(rk), np.array(lv), np.array(rv)
+
+
+@pytest.mark.parametrize("mode", ["rope", "absorbed"])
+def test_paged_decode_at_full_page_rank_is_softmax_attention_over_every_token(mode):
+    # exact page factors: factorised pages + dense tokens must be plain attention over all of them
+    rng = np.random.default_rng(62)
+    B, n, d_h, P, npg, D = 2, 3, 8, 4, 3, 5
+    keys = rng.standard_normal((B, npg * P + D, n, d_h))
+    vals = rng.standard_normal((B, npg * P + D, n, d_h))
+    q = rng.standard_normal((B, n, d_h))
+    f = [_pages_of(keys[b, :npg * P], vals[b, :npg * P], P, P) for b in range(B)]
+    lk, rk, lv, rv = (np.array([fb[k] for fb in f]) for k in range(4))
+    qp = [0, 0]        # q_pos 0: the rotation is the identity on the RoPE path
+    o_pg, o_den, lse = O.decode_paged(q, lk, rk, lv, rv, [npg, 2], keys[:, npg * P:], vals[:, npg * P:], [D, 3],
+                                      mode=mode, q_pos=qp)
+    for b, (used_pages, used_dense) in enumerate([(npg, D), (2, 3)]):
+        idx = list(range(used_pages * P)) + [npg * P + t for t in range(used_dense)]
+        for i in range(n):
+            sc = keys[b, idx, i] @ q[b, i] / math.sqrt(d_h)
+            p = scipy.special.softmax(sc)
+            np.testing.assert_allclose(o_pg[b, i] + o_den[b, i], p @ vals[b, idx, i], atol=1e-12)
+            np.testing.assert_allclose(o_den[b, i], p[used_pages * P:] @ vals[b, idx[used_pages * P:], i],
+                                       atol=1e-12)
+            assert abs(lse[b, i] - scipy.special.logsumexp(sc)) < 1e-12
+
+
+def test_paged_decode_rotates_the_query_like_the_dense_tokens():
+    # RoPE path: scores use q rotated at q_pos against keys as stored (already rotated)
+    rng = np.random.default_rng(63)
+    B, n, d_h, P = 1, 2, 4, 2
+    keys = rng.standard_normal((B, 2 * P, n, d_h))
+    vals = rng.standard_normal((B, 2 * P, n, d_h))
+    q = rng.standard_normal((B, n, d_h))
+    lk, rk, lv, rv = (a[None] for a in _pages_of(keys[0], vals[0], P, P))
+    o_pg, _, lse = O.decode_paged(q, lk, rk, lv, rv, [2], keys[:, :0], vals[:, :0], [0], mode="rope",
+                                  q_pos=[5])
+    for i in range(n):
+        # the rotation by complex multiplication of the rotate-half pairs (k, k + d_h/2)
+        w = O.rope_inv_freq(d_h, 10000.0)
+        z = (q[0, i, :2] + 1j * q[0, i, 2:]) * np.exp(1j * 5 * w)
+        qr = np.concatenate([z.real, z.imag])
+        sc = keys[0, :, i] @ qr / math.sqrt(d_h)
+        np.testing.assert_allclose(o_pg[0, i], scipy.special.softmax(sc) @ vals[0, :, i], atol=1e-12)
+        assert abs(lse[0, i] - scipy.special.logsumexp(sc)) < 1e-12
+
+
+def test_paged_decode_brute_force_low_rank():
+    # rank below the page size: scalar loops over the printed formula, s_p = (q R^T) L^T / sqrt(d)
+    rng = np.random.default_rng(64)
+    B, n, d_h, P, r, npg, D = 1, 2, 4, 3, 2, 2, 2
+    lk = rng.standard_normal((B, npg, n, P, r))
+    rk = rng.standard_normal((B, npg, n, r, d_h))
+    lv = rng.standard_normal((B, npg, n, P, r))
+    rv = rng.standard_normal((B, npg, n, r, d_h))
+    dk = rng.standard_normal((B, D, n, d_h))
+    dv = rng.standard_normal((B, D, n, d_h))
+    q = rng.standard_normal((B, n, d_h))
+    o_pg, o_den, lse = O.decode_paged(q, lk, rk, lv, rv, [npg], dk, dv, [D], mode="absorbed")
+    for i in range(n):
+        scores, vecs = [], []
+        for p in range(npg):
+            u = [math.fsum(q[0, i, e] * rk[0, p, i, j, e] for e in range(d_h)) for j in range(r)]
+            for t in range(P):
+                scores.append(math.fsum(u[j] * lk[0, p, i, t, j] for j in range(r)) / math.sqrt(d_h))
+                vecs.append([math.fsum(lv[0, p, i, t, j] * rv[0, p, i, j, e] for j in range(r)) for e in range(d_h)])
+        for t in range(D):
+            scores.append(math.fsum(q[0, i, e] * dk[0, t, i, e] for e in range(d_h)) / math.sqrt(d_h))
+            vecs.append(list(dv[0, t, i]))
+        m = max(scores)
+        ex = [math.exp(x - m) for x in scores]
+        l = math.fsum(ex)
+        full = [math.fsum(ex[t] * vecs[t][e] for t in range(len(ex))) / l for e in range(d_h)]
+        dense = [math.fsum(ex[t] * vecs[t][e] for t in range(npg * P, len(ex))) / l for e in range(d_h)]
+        np.testing.assert_allclose(o_pg[0, i] + o_den[0, i], full, atol=1e-12)
+        np.testing.assert_allclose(o_den[0, i], dense, atol=1e-12)
+        assert abs(lse[0, i] - (m + math.log(l))) < 1e-12
+
+
+def test_paged_decode_empty_row():
+    z5 = np.zeros((1, 1, 1, 2, 1))
+    zr = np.zeros((1, 1, 1, 1, 4))
+    o_pg, o_den, lse = O.decode_paged(np.ones((1, 1, 4)), z5, zr, z5, zr, [0], np.zeros((1, 0, 1, 4)),
+                                      np.zeros((1, 0, 1, 4)), [0], mode="absorbed")
+    assert np.all(o_pg == 0) and np.all(o_den == 0) and lse[0, 0] == -math.inf
+
+
+# ---------------------------------------------------------------------------
 # ALiBi on the absorbed path
 # ---------------------------------------------------------------------------
 
