@@ -748,6 +748,77 @@ def bench_hybrid(args, dev, flush, peaks, peaks_src, sinks=4, window=64):
     return e
 
 
+def bench_paged(args, dev, flush, peaks, peaks_src, sinks=4, window=64, page=32, rank=16):
+    """Decode over a page-factorised cache (PuzzleKV section 3.3) at the Llama-2-7B shape: batch 4,
+    32 heads, d_h 128, 64K tokens as `sinks` + `window` dense fp16 tokens and the rest in pages of 32
+    tokens stored as rank-16 fp16 factors (10 KB per page and head). Times the whole call (the paged
+    kernel and the dense merge); bound by HBM."""
+    import numpy as np
+    import torch
+    from oracle import palu_oracle as O
+    from rank_kv_cache_gb300 import palu as P
+    B, n, d_h, T = 4, 32, 128, 65536
+    D = sinks + window
+    n_pages = (T - D) // page
+    bk = torch.zeros((8, 256, 4 * d_h), dtype=torch.float16, device=dev)
+    attn = P.PaluAttention(bk, n_heads=n, head_dim=d_h, group_size=4, rank_k=256, rank_v=256, latent_dtype="f16",
+                           q_dtype="f16", mode="rope", max_batch=B, max_tokens=T, max_position=T)
+    g = torch.Generator(device=dev)
+    g.manual_seed(17)
+    rec = (torch.randn((B, n_pages, n, 320 * rank), generator=g, device=dev) * 0.2).half()
+    dk = torch.randn((B, D, n, d_h), generator=g, device=dev).half()
+    dv = torch.randn((B, D, n, d_h), generator=g, device=dev).half()
+    q = torch.randn((B, n, d_h), generator=g, device=dev).half()
+    npg = torch.full((B,), n_pages, dtype=torch.int32, device=dev)
+    nd = torch.full((B,), D, dtype=torch.int32, device=dev)
+    qp = torch.full((B,), T - 1, dtype=torch.int32, device=dev)
+    out = torch.empty((B, n, d_h), dtype=torch.float32, device=dev)
+    od = torch.empty((B, n, d_h), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, n), dtype=torch.float32, device=dev)
+
+    def call():
+        attn.decode_paged(q, rec, npg, max_pages=n_pages, q_pos=qp, dense_k=dk, dense_v=dv, dense_n=nd, out=out,
+                          out_dense=od, lse=lse)
+
+    for _ in range(5):
+        call()
+    torch.cuda.synchronize()
+    ms = event_times(call, 50, flush)
+    attn.check_device()
+    nbytes = rec.numel() * 2 + 2 * dk.numel() * 2
+    med = pct(ms, 50)
+    e = {"batch": B, "n_heads": n, "page_tokens": page, "rank": rank, "pages_per_row": n_pages,
+         "sink_tokens": sinks, "window_tokens": window, "dtype": "f16",
+         "kernels": ["paged_decode_kernel", "merge_dense_kernel"], "gpu_launches_per_step": 2,
+         "call_us": stats_us(ms), "bytes": nbytes, "roofline": hbm_roofline(nbytes, med, peaks, peaks_src)}
+    e["roofline"]["duration"] = "median whole call (paged decode + dense merge)"
+    # the oracle on one (row, head), against the same inputs
+    b1, h1 = 1, 7
+    r64 = rec[b1, :, h1].float().cpu().double().numpy()
+    o1, o2, o3 = page * rank, page * rank + rank * d_h, 2 * page * rank + rank * d_h
+    fk = (r64[:, :o1].reshape(1, n_pages, 1, page, rank), r64[:, o1:o2].reshape(1, n_pages, 1, rank, d_h),
+          r64[:, o2:o3].reshape(1, n_pages, 1, page, rank), r64[:, o3:].reshape(1, n_pages, 1, rank, d_h))
+    args64 = (q[b1:b1 + 1, h1:h1 + 1].cpu().double().numpy(), *fk, [n_pages],
+              dk[b1:b1 + 1, :, h1:h1 + 1].cpu().double().numpy(), dv[b1:b1 + 1, :, h1:h1 + 1].cpu().double().numpy(),
+              [D])
+    ref_p, ref_d, ref_lse = O.decode_paged(*args64, mode="rope", q_pos=[T - 1])
+    got = (out[b1, h1] + od[b1, h1]).cpu().double().numpy()
+    ref = ref_p[0, 0] + ref_d[0, 0]
+    e["parity_sample"] = {"heads": [[b1, h1]], "max_err_over_max_ref": float(np.abs(got - ref).max() / np.abs(ref).max()),
+                          "lse_abs_err": float(abs(lse[b1, h1].item() - ref_lse[0, 0]))}
+    if not args.no_cpu_baseline:
+        calls, sec = oracle_seconds(lambda: O.decode_paged(*args64, mode="rope", q_pos=[T - 1]), 2.0)
+        per_head = nbytes / (B * n)
+        e["cpu_baseline"] = {"value": round(per_head * calls / sec / 1e9, 4), "unit": "GB/s",
+                             "cores": _blas_threads(), "kind": "oracle", "seconds": round(sec, 2),
+                             "sample": f"{calls} decodes of one (row, head) over its {n_pages} pages and {D} dense "
+                                       "tokens (float64 NumPy)"}
+    attn.close()
+    del rec
+    torch.cuda.empty_cache()
+    return e
+
+
 VARIANTS = (
     # name, workload base, overrides, descriptor flags
     ("llama2-7b-rope-fp16k-int4v-b4-t64k", "ROPE_FP16", dict(batch=4, T=65536, v_dtype="int4"), 0),
@@ -789,6 +860,7 @@ def next_row_table():
     for name, base, over, flags in VARIANTS:
         t[name] = (lambda base, over, flags: lambda *a: bench_variant(*a, base, over, flags))(base, over, flags)
     t["llama2-7b-hybrid-int4-b4-t64k-s4-w64"] = lambda *a: bench_hybrid(*a)
+    t["puzzlekv-paged-fp16-b4-t64k-p32-r16-s4-w64"] = lambda *a: bench_paged(*a)
     for b, T, lat in ((1, 4096, "int4"), (4, 4096, "f16")):
         t[f"llama2-7b-prefill-{lat}-b{b}-t4k"] = (lambda b, T, lat: lambda *a: bench_prefill(*a, b, T, lat))(b, T, lat)
     return t

@@ -337,6 +337,46 @@ palu_status_t palu_decode_hybrid(palu_attn_t h, const void* q, const palu_cache*
                                  palu_stream_t stream);
 
 /*
+ * Decode over a page-factorised cache ("PuzzleKV" section 3.3, eq. 2 and step 4): every completed
+ * page of P tokens of a head stores its keys and values as rank-r factors, K_p ~= L_K R_K and
+ * V_p ~= L_V R_V (L: P x r with orthonormal columns from the page's truncated SVD, R: r x d_h).
+ * A page is scored as s = (q R_K^T) L_K^T / sqrt(d_h) and its values are read as p L_V R_V,
+ * without rebuilding the page. The dense sink and window tokens, when given, share the softmax.
+ * This is the PuzzleKV alternative to the G-LRD latent middle of palu_decode_hybrid; the handle
+ * supplies the heads, head_dim, q dtype, mode, RoPE table and workspace (its latent shape is not
+ * used).
+ *
+ *   pages->pages     device, 16-byte aligned: [max_rows][capacity][n_heads] page records, each
+ *                    L_K [P][r], R_K [r][head_dim], L_V [P][r], R_V [r][head_dim] row-major and
+ *                    contiguous (640 r bytes for P = 32, head_dim 128), in pages->dtype (F16/BF16).
+ *                    On the RoPE path the factorised keys are the stored, rotated keys.
+ *   pages->n_pages   device [batch] int32: pages 0 .. n_pages[b] - 1 of row b are attended; a
+ *                    count outside [0, max_pages] is clamped and recorded in the error word.
+ *   max_pages        bound on n_pages for this call (<= capacity); it sizes the split plan.
+ *   dense            NULL, or the sink / window tokens as for palu_decode_hybrid.
+ *   q                [batch][n_heads][head_dim] in the handle's q dtype, unrotated; q_pos [batch]
+ *                    is required on the RoPE path.
+ *   out              [batch][n_heads][head_dim]: sum over the pages of p (L_V R_V) (value space)
+ *   out_dense        [batch][n_heads][head_dim] when dense is given: sum over the dense tokens
+ *   lse              [batch][n_heads], required: natural log-sum-exp over all attended tokens
+ * so the attention output is out + out_dense. Supported: head_dim 128, P = 32, r in {8, 16, 32}
+ * (else PALU_ERR_UNSUPPORTED); PALU_FLAG_ALIBI handles are refused (no positions). One launch, two
+ * with the dense segment, asynchronous on `stream`.
+ */
+typedef struct palu_page_cache {
+  const void* pages;
+  const int32_t* n_pages;
+  int64_t capacity;
+  int page_size;
+  int rank;
+  palu_dtype_t dtype;
+} palu_page_cache;
+
+palu_status_t palu_decode_paged(palu_attn_t h, const void* q, const palu_page_cache* pages, const int32_t* q_pos,
+                                int batch, int64_t max_pages, const palu_dense_cache* dense, float* out,
+                                float* out_dense, float* lse, palu_stream_t stream);
+
+/*
  * Latent production: the step that fills the cache ("方法细节", SVD-rewrite paragraph: the
  * layer caches h = x A in place of k = x W and v = x W_v; G-LRD paragraph: one A_g per group;
  * "补充细节": per-token quantisation of the cached latents). For n_new new tokens of each

@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_lib")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_NAME = "libpalu_attn.so"
-SOURCES = ["palu_host.cu", "prep.cu", "decode_simt.cu", "decode_tc.cu", "decode_abs.cu", "noalloc.cu", "oproj.cu", "prefill.cu", "hybrid.cu"]
+SOURCES = ["palu_host.cu", "prep.cu", "decode_simt.cu", "decode_tc.cu", "decode_abs.cu", "noalloc.cu", "oproj.cu", "prefill.cu", "hybrid.cu", "paged.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

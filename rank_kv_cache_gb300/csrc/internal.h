@@ -139,6 +139,30 @@ struct DenseArgs {
 };
 cudaError_t launch_merge_dense(const DenseArgs& d, cudaStream_t st);
 
+// page-factorised decode (paged.cu): PuzzleKV pages of P = 32 tokens, d_h = 128, rank 8, 16 or 32
+struct PagedArgs {
+  const void* pages;          // [rows][capacity][n_heads] records: L_K [P][r], R_K [r][d], L_V [P][r], R_V [r][d]
+  const int32_t* n_pages;     // [batch] factorised pages per row
+  int64_t capacity;           // pages per row
+  int max_pages;              // bound on n_pages (this call)
+  int dtype;                  // kF16 or kBF16
+  int rank;
+  int n_heads;
+  int rope;                   // rotate the query at q_pos
+  const int32_t* q_pos;
+  const float2* rope_tab;     // [max_pos][d/2]
+  int64_t max_pos;
+  const void* q;
+  int q_dtype;
+  float qscale;               // log2(e) / sqrt(d)
+  int pages_per_split;
+  ErrWord* err;
+  uint64_t wait_ns;
+  DecodeArgs m;               // the split merge: batch, n_heads, n_splits, rv = d, part_o, part_ml, counters, out, lse
+};
+int paged_ctas_per_sm(int rank);
+cudaError_t launch_decode_paged(const PagedArgs& P, cudaStream_t st);
+
 // TMA-streaming absorbed-mode kernel (decode_abs.cu)
 bool abs_supported(const DecodeArgs& a);
 int abs_stage_tokens();

@@ -532,28 +532,11 @@ palu_status_t palu_decode_attn(palu_attn_t h, const void* q, const palu_cache* c
   return e == cudaSuccess ? PALU_OK : PALU_ERR_CUDA;
 }
 
-palu_status_t palu_decode_hybrid(palu_attn_t h, const void* q, const palu_cache* cache, const int32_t* seq_lens,
-                                 const int32_t* positions, const int32_t* q_pos, int batch, int64_t max_seq_len,
-                                 const palu_dense_cache* dense, float* out, float* out_dense, float* lse,
-                                 palu_stream_t stream) {
-  if (!h || !dense) return PALU_ERR_INVALID_ARG;
-  if (h->d.flags & PALU_FLAG_ALIBI) return PALU_ERR_UNSUPPORTED;   // the dense tokens carry no positions
-  if (h->d.head_dim > 128 || h->d.head_dim % 32) return PALU_ERR_UNSUPPORTED;
-  if (batch < 0 || batch > h->d.max_batch) return PALU_ERR_INVALID_ARG;
-  if (batch == 0) return PALU_OK;
-  if (!lse || !out_dense || (uintptr_t)out_dense % 4 || (uintptr_t)lse % 4) return PALU_ERR_INVALID_ARG;
-  if (h->d.mode == PALU_MODE_ROPE && !q_pos) return PALU_ERR_INVALID_ARG;
-  if (!dense->k || !dense->v || !dense->n_tokens || dense->capacity <= 0 || dense->capacity > (int64_t(1) << 31) ||
-      (unsigned)dense->dtype > PALU_BF16)
-    return PALU_ERR_INVALID_ARG;
-  // 16-bit rows are read four elements (8 bytes) at a time
-  const size_t al = dense->dtype == PALU_F32 ? 4 : 8;
-  if ((uintptr_t)dense->k % al || (uintptr_t)dense->v % al) return PALU_ERR_INVALID_ARG;
-  // the latent middle: out and lse hold its own softmax until the merge below
-  palu_status_t st = palu_decode_attn(h, q, cache, seq_lens, positions, q_pos, batch, max_seq_len, out, lse, stream);
-  if (st != PALU_OK) return st;
-  DecodeArgs a{};
-  fill_args(h, cache, batch, max_seq_len, a);
+// Dense sink / window segment of a hybrid call merged into `out` (the other segment's output and
+// lse), shared by palu_decode_hybrid's latent middle and palu_decode_paged's factorised pages.
+static palu_status_t merge_dense_segment(const palu_attn* h, const DecodeArgs& a, const palu_dense_cache* dense,
+                                         int batch, int out_width, const void* q, const int32_t* q_pos, float* out,
+                                         float* out_dense, float* lse, palu_stream_t stream) {
   DenseArgs d{};
   d.k = dense->k;
   d.v = dense->v;
@@ -562,7 +545,7 @@ palu_status_t palu_decode_hybrid(palu_attn_t h, const void* q, const palu_cache*
   d.capacity = dense->capacity;
   d.n_heads = h->d.n_heads;
   d.dh = h->d.head_dim;
-  d.rv = h->d.rank_v;
+  d.rv = out_width;
   d.batch = batch;
   d.rope = h->d.mode == PALU_MODE_ROPE;
   d.q_pos = q_pos;
@@ -577,6 +560,100 @@ palu_status_t palu_decode_hybrid(palu_attn_t h, const void* q, const palu_cache*
   d.err = a.err;
   const cudaError_t e = launch_merge_dense(d, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PALU_OK : PALU_ERR_CUDA;
+}
+
+static palu_status_t check_dense(const palu_dense_cache* dense) {
+  if (!dense->k || !dense->v || !dense->n_tokens || dense->capacity <= 0 || dense->capacity > (int64_t(1) << 31) ||
+      (unsigned)dense->dtype > PALU_BF16)
+    return PALU_ERR_INVALID_ARG;
+  // 16-bit rows are read four elements (8 bytes) at a time
+  const size_t al = dense->dtype == PALU_F32 ? 4 : 8;
+  if ((uintptr_t)dense->k % al || (uintptr_t)dense->v % al) return PALU_ERR_INVALID_ARG;
+  return PALU_OK;
+}
+
+palu_status_t palu_decode_hybrid(palu_attn_t h, const void* q, const palu_cache* cache, const int32_t* seq_lens,
+                                 const int32_t* positions, const int32_t* q_pos, int batch, int64_t max_seq_len,
+                                 const palu_dense_cache* dense, float* out, float* out_dense, float* lse,
+                                 palu_stream_t stream) {
+  if (!h || !dense) return PALU_ERR_INVALID_ARG;
+  if (h->d.flags & PALU_FLAG_ALIBI) return PALU_ERR_UNSUPPORTED;   // the dense tokens carry no positions
+  if (h->d.head_dim > 128 || h->d.head_dim % 32) return PALU_ERR_UNSUPPORTED;
+  if (batch < 0 || batch > h->d.max_batch) return PALU_ERR_INVALID_ARG;
+  if (batch == 0) return PALU_OK;
+  if (!lse || !out_dense || (uintptr_t)out_dense % 4 || (uintptr_t)lse % 4) return PALU_ERR_INVALID_ARG;
+  if (h->d.mode == PALU_MODE_ROPE && !q_pos) return PALU_ERR_INVALID_ARG;
+  palu_status_t st = check_dense(dense);
+  if (st != PALU_OK) return st;
+  // the latent middle: out and lse hold its own softmax until the merge below
+  st = palu_decode_attn(h, q, cache, seq_lens, positions, q_pos, batch, max_seq_len, out, lse, stream);
+  if (st != PALU_OK) return st;
+  DecodeArgs a{};
+  fill_args(h, cache, batch, max_seq_len, a);
+  return merge_dense_segment(h, a, dense, batch, h->d.rank_v, q, q_pos, out, out_dense, lse, stream);
+}
+
+palu_status_t palu_decode_paged(palu_attn_t h, const void* q, const palu_page_cache* pages, const int32_t* q_pos,
+                                int batch, int64_t max_pages, const palu_dense_cache* dense, float* out,
+                                float* out_dense, float* lse, palu_stream_t stream) {
+  if (!h || !pages) return PALU_ERR_INVALID_ARG;
+  if (h->d.flags & PALU_FLAG_ALIBI) return PALU_ERR_UNSUPPORTED;   // the pages carry no positions
+  if (h->d.head_dim != 128) return PALU_ERR_UNSUPPORTED;
+  if (pages->page_size != 32 || (pages->rank != 8 && pages->rank != 16 && pages->rank != 32) ||
+      (pages->dtype != PALU_F16 && pages->dtype != PALU_BF16))
+    return PALU_ERR_UNSUPPORTED;
+  if (batch < 0 || batch > h->d.max_batch) return PALU_ERR_INVALID_ARG;
+  if (batch == 0) return PALU_OK;
+  if (!q || (uintptr_t)q % 4 || !out || (uintptr_t)out % 4 || !lse || (uintptr_t)lse % 4) return PALU_ERR_INVALID_ARG;
+  if (!pages->pages || (uintptr_t)pages->pages % 16 || !pages->n_pages || pages->capacity <= 0) return PALU_ERR_INVALID_ARG;
+  if (max_pages < 0 || max_pages > pages->capacity || max_pages > (int64_t(1) << 30)) return PALU_ERR_INVALID_ARG;
+  if (h->d.mode == PALU_MODE_ROPE && !q_pos) return PALU_ERR_INVALID_ARG;
+  if (dense) {
+    const palu_status_t st = check_dense(dense);
+    if (st != PALU_OK) return st;
+    if (!out_dense || (uintptr_t)out_dense % 4) return PALU_ERR_INVALID_ARG;
+  }
+  if (cudaSetDevice(h->device) != cudaSuccess) return PALU_ERR_CUDA;
+  const int d_h = h->d.head_dim;
+  DecodeArgs a{};
+  palu_cache c{};
+  c.capacity = 1;
+  fill_args(h, &c, batch, 0, a);
+  a.rv = d_h;           // the merge's row: value-space outputs
+  a.out_rv = 0;
+  a.out = out;
+  a.lse = lse;
+  // split plan: like the decode kernels', in pages; partials of d_h floats must fit the workspace
+  int cap = h->L.max_splits * h->ks.rv / d_h;
+  if (cap > 256) cap = 256;
+  const int64_t units = (int64_t)batch * h->d.n_heads;
+  int n_splits = 1, per = (int)(max_pages > 0 ? max_pages : 1);
+  plan_splits(max_pages > 0 ? max_pages : 1, units, (int64_t)h->sm_count * paged_ctas_per_sm(pages->rank), cap, 8,
+              &n_splits, &per);
+  a.n_splits = n_splits;
+  PagedArgs P{};
+  P.pages = pages->pages;
+  P.n_pages = pages->n_pages;
+  P.capacity = pages->capacity;
+  P.max_pages = (int)max_pages;
+  P.dtype = to_dt(pages->dtype);
+  P.rank = pages->rank;
+  P.n_heads = h->d.n_heads;
+  P.rope = h->d.mode == PALU_MODE_ROPE;
+  P.q_pos = q_pos;
+  P.rope_tab = a.rope;
+  P.max_pos = a.max_pos;
+  P.q = q;
+  P.q_dtype = a.q_dtype;
+  P.qscale = a.qscale;
+  P.pages_per_split = per;
+  P.err = a.err;
+  P.wait_ns = a.wait_ns;
+  P.m = a;
+  cudaError_t e = launch_decode_paged(P, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return PALU_ERR_CUDA;
+  if (!dense) return PALU_OK;
+  return merge_dense_segment(h, a, dense, batch, d_h, q, q_pos, out, out_dense, lse, stream);
 }
 
 palu_status_t palu_debug_dequant(palu_attn_t h, const palu_cache* cache, int which, int batch, int64_t n_tokens,

@@ -35,7 +35,8 @@ EXPORTS = ("palu_attn_workspace_size", "palu_attn_create", "palu_append_latents"
            "palu_attn_trace_enable", "palu_attn_trace_read", "palu_decode_attn_noalloc", "palu_decode_plan",
            "palu_debug_int4_operand", "palu_debug_int4_dp2a", "palu_attn_trace_times",
            "palu_fuse_value_output", "palu_output_proj_workspace_size", "palu_output_proj",
-           "palu_down_proj_size", "palu_prepare_down_proj", "palu_project_latents", "palu_decode_hybrid")
+           "palu_down_proj_size", "palu_prepare_down_proj", "palu_project_latents", "palu_decode_hybrid",
+           "palu_decode_paged")
 PALU_TRACE_CAPACITY = 4096
 
 
@@ -56,6 +57,11 @@ class palu_cache(ctypes.Structure):
 class palu_dense_cache(ctypes.Structure):
     _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("n_tokens", ctypes.c_void_p),
                 ("capacity", ctypes.c_int64), ("dtype", ctypes.c_int)]
+
+
+class palu_page_cache(ctypes.Structure):
+    _fields_ = [("pages", ctypes.c_void_p), ("n_pages", ctypes.c_void_p), ("capacity", ctypes.c_int64),
+                ("page_size", ctypes.c_int), ("rank", ctypes.c_int), ("dtype", ctypes.c_int)]
 
 
 class PaluError(RuntimeError):
@@ -94,6 +100,8 @@ def _load():
         "palu_project_latents": (I, [P, P, I, I64, P, ctypes.POINTER(palu_cache), P, I, I, P]),
         "palu_decode_hybrid": (I, [P, P, ctypes.POINTER(palu_cache), P, P, P, I, I64,
                                    ctypes.POINTER(palu_dense_cache), P, P, P, P]),
+        "palu_decode_paged": (I, [P, P, ctypes.POINTER(palu_page_cache), P, I, I64,
+                                  ctypes.POINTER(palu_dense_cache), P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -222,6 +230,12 @@ def palu_prepare_down_proj(h, a_k: int, a_v: int, a_dtype: int, d_model: int, w_
 def palu_project_latents(h, w: int, w_dtype: int, d_model: int, x: int, cache: palu_cache, dst_slot: int,
                          batch: int, n_new: int, stream: int) -> int:
     return _lib.palu_project_latents(h, w, w_dtype, d_model, x, ctypes.byref(cache), dst_slot, batch, n_new, stream)
+
+
+def palu_decode_paged(h, q: int, pages: palu_page_cache, q_pos, batch: int, max_pages: int, dense, out: int,
+                      out_dense, lse: int, stream: int) -> int:
+    return _lib.palu_decode_paged(h, q, ctypes.byref(pages), q_pos, batch, max_pages,
+                                  ctypes.byref(dense) if dense is not None else None, out, out_dense, lse, stream)
 
 
 def palu_decode_hybrid(h, q: int, cache: palu_cache, seq_lens: int, positions, q_pos, batch: int,
@@ -374,6 +388,37 @@ class PaluAttention:
                                 B, int(max_seq_len), dense, _ptr(out), _ptr(out_dense), _ptr(lse),
                                 _stream_handle(stream))
         check(st, "palu_decode_hybrid")
+        return out, out_dense, lse
+
+    def decode_paged(self, q, pages, n_pages, *, max_pages, q_pos=None, dense_k=None, dense_v=None, dense_n=None,
+                     out=None, out_dense=None, lse=None, stream=None):
+        """Decode over a page-factorised cache (pages: a float16 / bfloat16 tensor [rows][capacity][n_heads]
+        [320 r] of page records L_K [32][r], R_K [r][128], L_V [32][r], R_V [r][128]; n_pages [batch]) and,
+        when dense_k is given, the dense sink / window tokens. Returns (out [B][n][d_h], out_dense or None,
+        lse [B][n])."""
+        torch = _torch()
+        _require_contiguous(q=q, pages=pages, n_pages=n_pages, q_pos=q_pos, dense_k=dense_k, dense_v=dense_v,
+                            dense_n=dense_n)
+        B = q.shape[0]
+        rec_bytes = pages[0, 0, 0].numel() * pages.element_size()
+        rank = rec_bytes // 640
+        if rec_bytes != 640 * rank:
+            raise ValueError("a page record holds 640 r bytes (P = 32, head_dim 128)")
+        pdt = {torch.float16: PALU_F16, torch.bfloat16: PALU_BF16}[pages.dtype]
+        pc = palu_page_cache(_ptr(pages), _ptr(n_pages), int(pages.shape[1]), 32, int(rank), pdt)
+        if out is None:
+            out = torch.empty((B, self.n_heads, self.head_dim), dtype=torch.float32, device=q.device)
+        if lse is None:
+            lse = torch.empty((B, self.n_heads), dtype=torch.float32, device=q.device)
+        dense = None
+        if dense_k is not None:
+            if out_dense is None:
+                out_dense = torch.empty((B, self.n_heads, self.head_dim), dtype=torch.float32, device=q.device)
+            ddt = {torch.float32: PALU_F32, torch.float16: PALU_F16, torch.bfloat16: PALU_BF16}[dense_k.dtype]
+            dense = palu_dense_cache(_ptr(dense_k), _ptr(dense_v), _ptr(dense_n), int(dense_k.shape[1]), ddt)
+        st = palu_decode_paged(self.handle, _ptr(q), pc, _ptr(q_pos), B, int(max_pages), dense, _ptr(out),
+                               _ptr(out_dense), _ptr(lse), _stream_handle(stream))
+        check(st, "palu_decode_paged")
         return out, out_dense, lse
 
     def prepare_down_proj(self, a_k, a_v, *, dtype="f16", stream=None):

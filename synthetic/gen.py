@@ -272,3 +272,35 @@ def storage_round(a, dtype: str):
 def hadamard_sylvester(r: int) -> np.ndarray:
     """Normalised Sylvester Walsh-Hadamard matrix (input preparation only)."""
     return scipy.linalg.hadamard(r).astype(np.float64) / math.sqrt(r)
+
+
+def page_factor_draw(seed: int, batch: int, n_pages: int, n_heads: int, page: int = 32, rank: int = 16,
+                     head_dim: int = 128, tau: float = 4.0, key_scale: float = 1.0):
+    """Seeded stand-ins for page-factorised keys and values (the PuzzleKV page cache, section 3.3):
+    L [B][pages][n][P][r] with orthonormal columns (QR of a Gaussian matrix, sign-fixed) and
+    R = diag(sigma) G [B][pages][n][r][d] with G's rows orthonormal and sigma_j = sqrt(P) exp(-j/tau),
+    the shape a page's truncated SVD has. Returns (lk, rk, lv, rv) as float32 arrays; nothing here
+    factorises or attends."""
+    rng = np.random.default_rng(np.random.SeedSequence([SEED_BASE, 7, seed]))
+    sig = math.sqrt(page) * np.exp(-np.arange(rank) / tau)
+
+    def draw(scale):
+        z = rng.standard_normal((batch, n_pages, n_heads, page, rank))
+        q, r = np.linalg.qr(z)
+        L = q * np.sign(np.diagonal(r, axis1=-2, axis2=-1))[..., None, :]
+        g = rng.standard_normal((batch, n_pages, n_heads, head_dim, rank))
+        qg, rg = np.linalg.qr(g)
+        G = np.swapaxes(qg * np.sign(np.diagonal(rg, axis1=-2, axis2=-1))[..., None, :], -1, -2)
+        return L.astype(np.float32), (scale * sig[:, None] * G).astype(np.float32)
+
+    lk, rk = draw(key_scale)
+    lv, rv = draw(1.0)
+    return lk, rk, lv, rv
+
+
+def page_records(lk, rk, lv, rv):
+    """Pack page factors into the library's record layout [B][pages][n][L_K | R_K | L_V | R_V]
+    (row-major, contiguous); pure reshaping."""
+    B, npg, n = lk.shape[:3]
+    parts = [np.reshape(a, (B, npg, n, -1)) for a in (lk, rk, lv, rv)]
+    return np.ascontiguousarray(np.concatenate(parts, axis=-1))
