@@ -495,6 +495,7 @@ def run_gpu(args, cfg, name):
     torch.cuda.empty_cache()
     if rank == 0 and world == 1 and not args.no_per_config:
         result["per_config"] = run_per_config(args, dev, flush, name, headline_entry, peaks, peaks_src)
+        result["t_sweep"] = run_t_sweep(args, dev, flush, peaks, peaks_src)
         result["next_rows"] = run_next_rows(args, dev, flush, peaks, peaks_src)
     if dist:
         dist.barrier()
@@ -557,6 +558,43 @@ def run_per_config(args, dev, flush, headline, headline_entry, peaks, peaks_src)
         wl.close()
         del wl
         torch.cuda.empty_cache()
+    return out
+
+
+# T sweep: each 64K workload's decode at T = 4K, 8K, 16K, 32K and 64K (same batch and layer)
+T_SWEEP = (4096, 8192, 16384, 32768, 65536)
+T_SWEEP_WORKLOADS = ("llama2-7b-rope-int4-hadamard-b4-t64k", "llama2-7b-absorbed-fp16-b4-t64k")
+
+
+def run_t_sweep(args, dev, flush, peaks, peaks_src):
+    """The decode kernel of each T_SWEEP_WORKLOADS workload at every T of T_SWEEP: 5 warm-up steps,
+    then 30 timed steps (100 at T <= 8K), L2 flushed before each; median decode kernel, latent and
+    dense-equivalent GB/s, and the roofline fraction."""
+    import torch
+    out = {}
+    for name in T_SWEEP_WORKLOADS:
+        rows = []
+        for T in T_SWEEP:
+            cfg = config_of(name, tokens=T)
+            wl = GpuWorkload(cfg, dev)
+            for _ in range(5):
+                flush.zero_()
+                wl.step()
+            torch.cuda.synchronize()
+            _, kms, _ = timed_steps(wl, 100 if T <= 8192 else 30, flush)
+            work = step_work(cfg)
+            med = pct(kms, 50)
+            roof = roofline_for(cfg, work, med, peaks, peaks_src, long_step=False)
+            rows.append({"tokens": T, "n_splits": wl.plan()[1], "decode_kernel_us": round(med * 1e3, 2),
+                         "latent_gbs": round(work["decode_bytes"] / (med / 1e3) / 1e9, 1),
+                         "dense_equiv_gbs": round(work["dense_fp16_kv_bytes"] / (med / 1e3) / 1e9, 1),
+                         "bound": roof["bound"], "frac": roof["frac"]})
+            wl.close()
+            del wl
+            torch.cuda.empty_cache()
+        out[name] = rows
+        print(f"[bench] T sweep {name}: " + ", ".join(f"{r['tokens'] // 1024}K {r['decode_kernel_us']} us "
+                                                     f"({r['frac']})" for r in rows), file=sys.stderr, flush=True)
     return out
 
 
