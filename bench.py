@@ -104,15 +104,32 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+GB300_SMS = 152
+FP32_LANES_PER_SM = 128
+
+
+def alu_peak_tflops(peaks):
+    """fp32 FMA peak of the CUDA cores: 152 SMs x 128 lanes x 2 flops x the maximum SM clock."""
+    return GB300_SMS * FP32_LANES_PER_SM * 2 * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
+
+
 def roofline_for(cfg, work, kernel_ms, peaks, peaks_src, long_step):
-    """The slower of latent bytes over HBM and (RoPE) rebuild flops over the tensor peak bounds
-    the decode kernel; achieved = that resource's algorithmic work / the kernel's duration."""
+    """The slowest of latent bytes over HBM, (RoPE) rebuild flops over the tensor peak and
+    (absorbed) score and p.H_v flops over the CUDA cores' fp32 peak bounds the decode kernel;
+    achieved = that resource's algorithmic work / the kernel's duration."""
     hbm = float(peaks["hbm_gbs"])
     tc_key = "bf16_tflops_sustained" if long_step else "bf16_tflops"
     tc = float(peaks[tc_key])  # fp16 = bf16 nominal rate
     t_hbm = work["decode_bytes"] / (hbm * 1e9)
     t_tc = work["flops"] / (tc * 1e12) if cfg.mode == "rope" else 0.0
     sec = kernel_ms / 1e3
+    alu = alu_peak_tflops(peaks)
+    t_alu = work["flops"] / (alu * 1e12) if cfg.mode != "rope" else 0.0
+    if t_alu > t_hbm:
+        ach = work["flops"] / sec / 1e12
+        return {"bound": "alu", "achieved": round(ach, 2), "peak": round(alu, 1), "unit": "TFLOP/s",
+                "frac": round(ach / alu, 4), "traffic": None, "roofline_us": round(t_alu * 1e6, 2),
+                "peak_source": f"152 SMs x 128 fp32 lanes x 2 x sm_max_mhz of {peaks_src}"}
     if t_tc > t_hbm:
         ach = work["flops"] / sec / 1e12
         return {"bound": "tensor", "achieved": round(ach, 2), "peak": tc, "unit": "TFLOP/s",
@@ -866,6 +883,8 @@ VARIANTS = (
     ("llama2-7b-rope-fp16-glrd-s4-r256-b1-t4k", "ROPE_FP16", dict(), 0),
     ("llama2-7b-rope-fp16-glrd-s8-r256-b1-t4k", "ROPE_FP16", dict(group_size=8), 0),
     ("llama2-7b-rope-fp16-jlrd-s32-r256-b1-t4k", "ROPE_FP16", dict(group_size=32), 0),
+    ("llama2-7b-absorbed-fp16-glrd-s8-b4-t64k", "ABSORBED_FP16", dict(group_size=8), 0),
+    ("llama2-7b-absorbed-fp16-jlrd-s32-b4-t64k", "ABSORBED_FP16", dict(group_size=32), 0),
 )
 
 

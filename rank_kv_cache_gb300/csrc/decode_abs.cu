@@ -118,6 +118,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int t_end = min(T, t_begin + span);
   const int n_stages = t_end > t_begin ? (t_end - t_begin + kStageTok - 1) / kStageTok : 0;
   const int head0 = g * kHeads;
+  const int cache_g = a.g_split > 1 ? g / a.g_split : g;   // split groups share their cache group's latents
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -145,8 +146,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::mbar_arrive_expect_tx(&full[s], kStageBytes);
         const int r = row0 + t_begin + i * kStageTok;
-        tc::tma_load_3d(smem + kOffRing + s * kStageBytes, &tm_hk, &full[s], 0, g, r);
-        tc::tma_load_3d(smem + kOffRing + s * kStageBytes + kHalfStage, &tm_hv, &full[s], 0, g, r);
+        tc::tma_load_3d(smem + kOffRing + s * kStageBytes, &tm_hk, &full[s], 0, cache_g, r);
+        tc::tma_load_3d(smem + kOffRing + s * kStageBytes + kHalfStage, &tm_hv, &full[s], 0, cache_g, r);
         ++issued;
       }
       if (!ok) {
@@ -340,8 +341,10 @@ cudaError_t launch_decode_abs(const DecodeArgs& a, cudaStream_t st) {
   CUtensorMap tm[2];
   const void* base[2] = {a.hk, a.hv};
   for (int i = 0; i < 2; ++i) {
-    const cuuint64_t dims[3] = {(cuuint64_t)kRank, (cuuint64_t)a.n_g, (cuuint64_t)a.batch * a.capacity};
-    const cuuint64_t strides[2] = {(cuuint64_t)kRank * 2, (cuuint64_t)a.n_g * kRank * 2};
+    // the cache's own groups: split groups (g_split > 1) share one cache group
+    const int cache_n_g = a.g_split > 1 ? a.n_g / a.g_split : a.n_g;
+    const cuuint64_t dims[3] = {(cuuint64_t)kRank, (cuuint64_t)cache_n_g, (cuuint64_t)a.batch * a.capacity};
+    const cuuint64_t strides[2] = {(cuuint64_t)kRank * 2, (cuuint64_t)cache_n_g * kRank * 2};
     const cuuint32_t box[3] = {(cuuint32_t)kRank, 1, (cuuint32_t)kStageTok};
     const cuuint32_t es[3] = {1, 1, 1};
     if (enc(&tm[i], dt, 3, const_cast<void*>(base[i]), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,

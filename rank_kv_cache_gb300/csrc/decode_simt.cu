@@ -61,17 +61,20 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(DecodeArgs a) {
 #pragma unroll
   for (int k = 0; k < kAccMax; ++k) acc[k] = 0.f;
 
+  // the cache group this kernel group reads (split groups share their cache group's latents)
+  const int gs = a.g_split > 1 ? a.g_split : 1;
+  const int cache_g = g / gs, cache_n_g = a.n_g / gs;
   for (int t0 = t_begin; t0 < t_end; t0 += TT) {
     const int nt = min(TT, t_end - t0);
     __syncthreads();
     for (int i = tid; i < TT * rk; i += kThreads) {
       const int t = i / rk, c = i % rk;
-      const int64_t row = ((int64_t)b * a.capacity + (t0 + t)) * a.n_g + g;
+      const int64_t row = ((int64_t)b * a.capacity + (t0 + t)) * cache_n_g + cache_g;
       hk_s[i] = (t < nt) ? Latent<KT>::get(a.hk, a.k_scale, row, rk, c) : 0.f;
     }
     for (int i = tid; i < TT * rv; i += kThreads) {
       const int t = i / rv, c = i % rv;
-      const int64_t row = ((int64_t)b * a.capacity + (t0 + t)) * a.n_g + g;
+      const int64_t row = ((int64_t)b * a.capacity + (t0 + t)) * cache_n_g + cache_g;
       hv_s[i] = (t < nt) ? Latent<VT>::get(a.hv, a.v_scale, row, rv, c) : 0.f;
     }
     __syncthreads();

@@ -55,6 +55,10 @@ struct DecodeArgs {
   // its own source group, columns ((h % 4) / pack_s) * out_rv + [0, out_rv).
   int out_rv;
   int pack_s;
+  // Split groups (g_split > 1, absorbed path): each cache group of g_split * 4 heads is run as g_split
+  // kernel groups of four heads over the same latents; kernel group g reads cache group g / g_split
+  // of the n_g / g_split in the cache.
+  int g_split;
   // failure-detection test hook (PALU_FLAG_TEST_STALL): the tensor-core kernel's H_v
   // producer issues nothing; wait_ns bounds every mbarrier wait of that kernel
   int test_stall;
@@ -66,7 +70,8 @@ struct DecodeArgs {
 // create-time set-up
 cudaError_t launch_rope_table(float2* tab, uint64_t* phase, int64_t max_pos, int dh, double theta, cudaStream_t st);
 cudaError_t launch_copy_bk(const void* src, int bk_dtype, void* dst, void* dst_t, int mma_dtype, int n_g,
-                           int rk, int cols, int dh, int perm8, int pack, int src_s, int src_rk, cudaStream_t st);
+                           int rk, int cols, int dh, int perm8, int pack, int split, int src_s, int src_rk,
+                           cudaStream_t st);
 
 // per-call kernels
 cudaError_t launch_qprep(int mode, const void* q, int q_dtype, const DecodeArgs& a, const int32_t* q_pos,

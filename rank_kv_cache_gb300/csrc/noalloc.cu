@@ -54,6 +54,7 @@ extern "C" palu_status_t palu_decode_attn_noalloc(const palu_attn_desc* desc, co
   palu_status_t st = palu_attn_workspace_size(desc, &ws_unused);  // validates the descriptor
   if (st != PALU_OK) return st;
   if (desc->mode != PALU_MODE_ABSORBED) return PALU_ERR_UNSUPPORTED;
+  if (desc->group_size > 8) return PALU_ERR_UNSUPPORTED;   // the CUDA-core kernel takes up to 8 heads a group
   if (desc->flags & PALU_FLAG_ALIBI) return PALU_ERR_UNSUPPORTED;   // this entry point takes no positions
   if (batch < 0 || batch > desc->max_batch) return PALU_ERR_INVALID_ARG;
   if (batch == 0) return PALU_OK;

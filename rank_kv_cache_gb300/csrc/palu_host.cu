@@ -44,7 +44,10 @@ palu_status_t check_desc(const palu_attn_desc* d) {
   // Llama-2-7B layer) only on the tensor-core RoPE kernel, whose shape rules they must meet
   const bool tc_shape = d->mode == PALU_MODE_ROPE && d->head_dim == 128 && d->rank_k == 256 && d->rank_v == 256 &&
                         (d->k_dtype == PALU_F16 || d->k_dtype == PALU_BF16 || d->k_dtype == PALU_INT4);
-  if (!pow2_in(d->group_size, 1, 8) && !(tc_shape && (d->group_size == 16 || d->group_size == 32)))
+  // ... and on the absorbed path as split groups (rank 256, fp16 / bf16 latents)
+  const bool split_shape = d->mode == PALU_MODE_ABSORBED && d->rank_k == 256 && d->rank_v == 256 &&
+                           d->k_dtype == d->v_dtype && (d->k_dtype == PALU_F16 || d->k_dtype == PALU_BF16);
+  if (!pow2_in(d->group_size, 1, 8) && !((tc_shape || split_shape) && (d->group_size == 16 || d->group_size == 32)))
     return PALU_ERR_UNSUPPORTED;
   if (!pow2_in(d->rank_k, 64, 256) || !pow2_in(d->rank_v, 64, 256)) return PALU_ERR_UNSUPPORTED;
   // one latent dtype for keys and values, or int4 values under fp16 / bf16 keys (V-only int4)
@@ -62,13 +65,24 @@ palu_status_t check_desc(const palu_attn_desc* d) {
 // scores then equal its own group's exactly (the other groups' latents meet zeros); its output
 // is the slice of the packed group's 256 latent columns that holds its own group's ranks, which
 // the split merge writes. This puts those shapes on the tensor-core and TMA-streamed kernels.
+// On the absorbed path, groups of 8, 16 or 32 heads at 256 ranks (fp16/bf16) are split the other
+// way: each runs as s / 4 kernel groups of four heads that read the same cache group, each with its
+// own column block of B_k, so the TMA-streamed kernel (four heads per CTA) takes them too.
 struct KShape {
   int s, rk, rv, pack;   // pack = source groups per kernel group (1: none)
+  int split;             // kernel groups per source group (1: none)
   int64_t n_g;
 };
 
 KShape kernel_shape(const palu_attn_desc& d) {
-  KShape k{d.group_size, d.rank_k, d.rank_v, 1, d.n_heads / d.group_size};
+  KShape k{d.group_size, d.rank_k, d.rank_v, 1, 1, d.n_heads / d.group_size};
+  if (d.mode == PALU_MODE_ABSORBED && (d.group_size == 8 || d.group_size == 16 || d.group_size == 32) &&
+      d.rank_k == 256 && d.rank_v == 256 && d.k_dtype == d.v_dtype && (d.k_dtype == PALU_F16 || d.k_dtype == PALU_BF16)) {
+    k.split = d.group_size / 4;
+    k.s = 4;
+    k.n_g = d.n_heads / 4;
+    return k;
+  }
   if ((d.group_size == 1 || d.group_size == 2) && d.head_dim == 128 && d.rank_k == 64 * d.group_size &&
       d.rank_v == d.rank_k && d.n_heads % 4 == 0 && d.k_dtype == d.v_dtype &&
       (d.k_dtype == PALU_F16 || d.k_dtype == PALU_BF16)) {
@@ -226,7 +240,7 @@ palu_status_t palu_attn_create(const palu_attn_desc* desc, const void* B_k, void
   void* bkt = (desc->mode == PALU_MODE_ROPE && desc->k_dtype != PALU_F32) ? h->ws + L.bkt : nullptr;
   if (e == cudaSuccess)
     e = launch_copy_bk(B_k, to_dt(desc->bk_dtype), h->ws + L.bk, bkt, h->mma_dtype, (int)k.n_g, k.rk,
-                       k.s * desc->head_dim, desc->head_dim, desc->k_dtype == PALU_INT4 ? 1 : 0, k.pack,
+                       k.s * desc->head_dim, desc->head_dim, desc->k_dtype == PALU_INT4 ? 1 : 0, k.pack, k.split,
                        desc->group_size, desc->rank_k, s);
   if (e == cudaSuccess && desc->mode == PALU_MODE_ROPE)
     e = launch_rope_table(reinterpret_cast<float2*>(h->ws + L.rope), reinterpret_cast<uint64_t*>(h->ws + L.phase),
@@ -434,6 +448,7 @@ static void fill_args(const palu_attn* h, const palu_cache* cache, int batch, in
   a.rv = h->ks.rv;
   a.out_rv = h->ks.pack > 1 ? d.rank_v : 0;   // packed groups: the merge writes each head's own slice
   a.pack_s = d.group_size;
+  a.g_split = h->ks.split;
   a.k_dtype = to_dt(d.k_dtype);
   a.v_dtype = to_dt(d.v_dtype);
   a.bk_dtype = to_dt(d.bk_dtype);
@@ -519,7 +534,7 @@ palu_status_t palu_decode_attn(palu_attn_t h, const void* q, const palu_cache* c
   const int kernel = plan_decode(h, a);
   const bool use_tc = kernel == PALU_KERNEL_TC_ROPE, use_abs = kernel == PALU_KERNEL_TMA_ABSORBED;
   // group sizes above 8 have no CUDA-core kernel (a cache of fewer than 128 rows in all)
-  if (kernel == PALU_KERNEL_SIMT && h->d.group_size > 8) return PALU_ERR_UNSUPPORTED;
+  if (kernel == PALU_KERNEL_SIMT && h->ks.s > 8) return PALU_ERR_UNSUPPORTED;
 
   // the tensor-core kernel rotates its query itself; the other kernels read the prepared buffer
   cudaError_t e = use_tc ? cudaSuccess

@@ -51,8 +51,10 @@ cudaError_t launch_rope_table(float2* tab, uint64_t* phase, int64_t max_pos, int
 // pack > 1 (packed groups, 16-bit B_k only): the n_g x rk x cols copy is the block-diagonal B_k of
 // kernel groups made of `pack` source groups of src_s heads and src_rk ranks: source group jg of
 // kernel group g fills ranks [jg src_rk, (jg + 1) src_rk) x its own heads' columns, zeros elsewhere.
+// split > 1 (split groups): kernel group g is column block g % split (cols wide) of source group
+// g / split, whose rows hold src_s * dh columns.
 __global__ void copy_bk_kernel(const void* src, int bk_dtype, void* dst, void* dst_t, int mma_dtype, int n_g,
-                               int rk, int cols, int dh, int perm8, int pack, int src_s, int src_rk) {
+                               int rk, int cols, int dh, int perm8, int pack, int split, int src_s, int src_rk) {
   const int64_t n = (int64_t)n_g * rk * cols;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
     const int c = int(i % cols);
@@ -61,6 +63,7 @@ __global__ void copy_bk_kernel(const void* src, int bk_dtype, void* dst, void* d
     const int esz = bk_dtype == kF32 ? 4 : 2;
     // the source element: the same index, or for packed groups the block-diagonal expansion
     int64_t si = i;
+    if (split > 1) si = ((int64_t)(g / split) * rk + m) * ((int64_t)src_s * dh) + (int64_t)(g % split) * cols + c;
     if (pack > 1) {
       const int jg = (c / dh) / src_s;   // source group of this column within the kernel group
       si = (m / src_rk == jg) ? (((int64_t)g * pack + jg) * src_rk + (m - jg * src_rk)) * ((int64_t)src_s * dh) +
@@ -83,11 +86,11 @@ __global__ void copy_bk_kernel(const void* src, int bk_dtype, void* dst, void* d
 }
 
 cudaError_t launch_copy_bk(const void* src, int bk_dtype, void* dst, void* dst_t, int mma_dtype, int n_g, int rk,
-                           int cols, int dh, int perm8, int pack, int src_s, int src_rk, cudaStream_t st) {
+                           int cols, int dh, int perm8, int pack, int split, int src_s, int src_rk, cudaStream_t st) {
   const int64_t n = (int64_t)n_g * rk * cols;
   const int blocks = int((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
-  copy_bk_kernel<<<blocks, 256, 0, st>>>(src, bk_dtype, dst, dst_t, mma_dtype, n_g, rk, cols, dh, perm8, pack, src_s,
-                                         src_rk);
+  copy_bk_kernel<<<blocks, 256, 0, st>>>(src, bk_dtype, dst, dst_t, mma_dtype, n_g, rk, cols, dh, perm8, pack, split,
+                                         src_s, src_rk);
   return cudaGetLastError();
 }
 

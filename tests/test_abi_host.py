@@ -92,7 +92,10 @@ def test_flags_accepted_per_mode():
     (dict(group_size=1, rank_k=64, rank_v=64), P.PALU_OK),            # M-LRD
     (dict(group_size=32), P.PALU_OK),                                 # J-LRD on the tensor-core path
     (dict(group_size=16, latent_dtype="int4"), P.PALU_OK),
-    (dict(group_size=32, mode="absorbed"), P.PALU_ERR_UNSUPPORTED),
+    (dict(group_size=32, mode="absorbed"), P.PALU_OK),                # J-LRD absorbed as split groups
+    (dict(group_size=16, mode="absorbed", latent_dtype="bf16"), P.PALU_OK),
+    (dict(group_size=32, mode="absorbed", latent_dtype="int4"), P.PALU_ERR_UNSUPPORTED),
+    (dict(group_size=16, mode="absorbed", rank_k=128, rank_v=128), P.PALU_ERR_UNSUPPORTED),
     (dict(group_size=32, rank_k=128, rank_v=128), P.PALU_ERR_UNSUPPORTED),
     (dict(group_size=32, latent_dtype="f32", q_dtype="f32"), P.PALU_ERR_UNSUPPORTED),
     (dict(group_size=64, n_heads=64), P.PALU_ERR_UNSUPPORTED),

@@ -111,3 +111,24 @@ def test_bad_arguments_are_refused():
         attn.decode_paged(q, rec[..., :100].contiguous(), npg, max_pages=2, q_pos=qp)
     torch.cuda.synchronize()
     attn.close()
+
+
+def test_page_count_above_the_bound_is_clamped_and_recorded():
+    import torch
+    from rank_kv_cache_gb300 import palu as P
+    B, cap, rank = 1, 6, 8
+    lk, rk, lv, rv = gen.page_factor_draw(9, B, cap, N_HEADS, rank=rank)
+    lk, rk, lv, rv = (gen.storage_round(a, "f16").float().numpy() for a in (lk, rk, lv, rv))
+    rec = gen.storage_round(gen.page_records(lk, rk, lv, rv), "f16").to("cuda")
+    q = gen.storage_round(np.random.default_rng(9).standard_normal((B, N_HEADS, D_H)), "f16")
+    attn = _handle("absorbed")
+    npg = torch.tensor([cap + 5], dtype=torch.int32, device="cuda")     # more pages than the call's bound
+    out, _, lse = attn.decode_paged(q.to("cuda"), rec, npg, max_pages=cap)
+    torch.cuda.synchronize()
+    with pytest.raises(P.PaluError) as e:
+        attn.check_device()
+    assert e.value.status == P.PALU_ERR_DEVICE
+    ref_p, _, ref_lse = O.decode_paged(q.double().numpy(), lk, rk, lv, rv, [cap], np.zeros((B, 0, N_HEADS, D_H)),
+                                       np.zeros((B, 0, N_HEADS, D_H)), [0], mode="absorbed")
+    assert_close(out.cpu().double().numpy(), ref_p, lse.cpu().double().numpy(), ref_lse)
+    attn.close()

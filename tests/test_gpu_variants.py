@@ -108,6 +108,22 @@ def test_joint_decomposition_j_lrd():
     _check(c)
 
 
+# G-LRD with s = 8, 16 and J-LRD (s = 32) at rank 256 on the absorbed path run as split groups: four
+# heads per kernel group over their group's shared latents, on the TMA-streamed kernel
+@pytest.mark.parametrize("lat,s,T,batch,seqs,qs,alibi", [
+    ("f16", 8, 300, 2, [300, 150], 1.0, False),
+    ("bf16", 16, 129, 2, [129, 64], 8.0, False),
+    ("f16", 32, 1000, 1, [1000], 1.0, True),
+    ("f16", 8, 40, 1, [40], 1.0, False),             # fewer than 64 cache rows: CUDA-core kernel
+])
+def test_split_groups_on_the_absorbed_path(lat, s, T, batch, seqs, qs, alibi):
+    from rank_kv_cache_gb300 import palu as P
+    cfg = gen.ABSORBED_FP16.with_(T=T, batch=batch, group_size=s, latent_dtype=lat)
+    c = Case(cfg, seq_lens=seqs, q_scale=qs, alibi=alibi)
+    assert _kernel(c) == (P.PALU_KERNEL_TMA_ABSORBED if batch * T >= 64 else P.PALU_KERNEL_SIMT)
+    _check(c)
+
+
 # ---------------------------------------------------------------- ALiBi on the absorbed path
 
 @pytest.mark.parametrize("dt", ["f16", "bf16"])
