@@ -96,7 +96,9 @@ typedef struct palu_attn_desc {
                              s = 1 or 2 with ranks 64 s, head_dim 128, F16/BF16 latents and
                              n_heads % 4 == 0 run packed four heads at a time with a block-diagonal
                              B_k (the workspace then holds 4 / s times the B_k bytes); the output
-                             layout is unchanged ([batch][n_heads][rank_v]) */
+                             layout is unchanged ([batch][n_heads][rank_v]). On the absorbed path
+                             s = 8, 16 or 32 at ranks 256 with F16/BF16 latents run as s / 4 groups
+                             of four heads over the same cached latents */
   int rank_k;             /* r_k per group: 64, 128 or 256 */
   int rank_v;             /* r_v per group: 64, 128 or 256 */
   palu_dtype_t k_dtype;   /* key-latent storage */
