@@ -362,8 +362,10 @@ palu_status_t palu_decode_hybrid(palu_attn_t h, const void* q, const palu_cache*
  *   out_dense        [batch][n_heads][head_dim] when dense is given: sum over the dense tokens
  *   lse              [batch][n_heads], required: natural log-sum-exp over all attended tokens
  * so the attention output is out + out_dense. Supported: head_dim 128, P = 32, r in {8, 16, 32}
- * (else PALU_ERR_UNSUPPORTED); PALU_FLAG_ALIBI handles are refused (no positions). One launch, two
- * with the dense segment, asynchronous on `stream`.
+ * (else PALU_ERR_UNSUPPORTED); PALU_FLAG_ALIBI handles are refused (no positions). The split partials
+ * live in the handle's workspace; a handle too small for one head_dim-wide partial per (row, head)
+ * (rank_v below head_dim with max_tokens <= 16) gives PALU_ERR_WORKSPACE. One launch, two with the
+ * dense segment, asynchronous on `stream`.
  */
 typedef struct palu_page_cache {
   const void* pages;

@@ -641,6 +641,7 @@ palu_status_t palu_decode_paged(palu_attn_t h, const void* q, const palu_page_ca
   // split plan: like the decode kernels', in pages; partials of d_h floats must fit the workspace
   int cap = h->L.max_splits * h->ks.rv / d_h;
   if (cap > 256) cap = 256;
+  if (cap < 1) return PALU_ERR_WORKSPACE;   // a handle whose partials cannot hold one d_h-wide split
   const int64_t units = (int64_t)batch * h->d.n_heads;
   int n_splits = 1, per = (int)(max_pages > 0 ? max_pages : 1);
   plan_splits(max_pages > 0 ? max_pages : 1, units, (int64_t)h->sm_count * paged_ctas_per_sm(pages->rank), cap, 8,
