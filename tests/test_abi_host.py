@@ -126,3 +126,28 @@ def test_status_strings():
     for s in range(7):
         assert P.palu_status_string(s)
     assert "unknown" in P.palu_status_string(99)
+
+
+def test_noalloc_refuses_groups_above_eight_heads_before_any_cuda_call():
+    # split groups exist only on the workspace path; the fixed-scratch entry point runs the
+    # CUDA-core kernel, which takes up to eight heads a group
+    for s in (16, 32):
+        d = _desc(mode="absorbed", group_size=s)
+        assert P.palu_attn_workspace_size(d)[0] == P.PALU_OK
+        st = P.palu_decode_attn_noalloc(d, 0x1000, 0x1000, P.palu_cache(), 0x1000, 1, 16, 0x1000, None, 0)
+        assert st == P.PALU_ERR_UNSUPPORTED
+
+
+def test_packed_and_split_group_workspaces():
+    # packed M-LRD / s = 2 groups are laid out as G-LRD groups of four heads at rank 256 (block-diagonal
+    # B_k, 256-wide partials); split absorbed groups keep the source B_k bytes in four-head blocks
+    _, s4 = P.palu_attn_workspace_size(_desc())
+    for s in (1, 2):
+        _, packed = P.palu_attn_workspace_size(_desc(group_size=s, rank_k=64 * s, rank_v=64 * s))
+        assert packed == s4
+    _, unpacked = P.palu_attn_workspace_size(_desc(group_size=1, rank_k=64, rank_v=64, latent_dtype="f32",
+                                                    q_dtype="f32"))
+    assert unpacked < s4
+    _, a4 = P.palu_attn_workspace_size(_desc(mode="absorbed"))
+    for s in (8, 16, 32):
+        assert P.palu_attn_workspace_size(_desc(mode="absorbed", group_size=s))[1] == a4
