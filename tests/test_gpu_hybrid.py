@@ -93,6 +93,13 @@ def test_absorbed_middle_with_dense_segment():
     _check(_run(cfg, [333, 100], [SINKS + WINDOW, 20], seed=3))
 
 
+@pytest.mark.parametrize("s,rank", [(1, 64), (8, 256)])
+def test_absorbed_packed_and_split_groups_with_dense_segment(s, rank):
+    # M-LRD packed four heads at a time, and s = 8 split into four-head groups, under the dense merge
+    cfg = gen.ABSORBED_FP16.with_(T=400, batch=2, group_size=s, rank=rank)
+    _check(_run(cfg, [400, 97], [SINKS + WINDOW, 2], seed=7))
+
+
 def test_empty_middle_empty_dense_and_both_empty():
     cfg = gen.ROPE_FP16.with_(T=200, batch=3)
     out, out_d, lse, ref_l, ref_d, ref_lse = _run(cfg, [0, 200, 0], [SINKS + WINDOW, 0, 0], seed=4)

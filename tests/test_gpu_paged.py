@@ -76,6 +76,10 @@ def test_absorbed_bf16_pages_without_dense_tokens():
     _check(_run("absorbed", "bf16", 8, [33, 1, 0], [0, 0, 0], seed=2))
 
 
+def test_rope_bf16_pages_rank32_fp32_dense_peaked():
+    _check(_run("rope", "bf16", 32, [70, 23], [68, 40], seed=6, q_scale=6.0, dense_dtype="f32"))
+
+
 def test_peaked_softmax_fp16_rank16():
     _check(_run("rope", "f16", 16, [64, 9], [68, 68], seed=3, q_scale=8.0))
 
