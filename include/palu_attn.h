@@ -37,6 +37,11 @@
  * given stream has finished. The library allocates no device memory: scratch
  * lives in the caller-provided workspace. A handle owns host memory only.
  *
+ * Concurrency: the decode calls of one handle (palu_decode_attn, _hybrid, _paged)
+ * share its workspace (split partials, the split-merge counters, the error word);
+ * calls that may overlap on the GPU need one handle, with its own workspace, each.
+ * Calls queued on one stream are ordered and safe.
+ *
  * Errors: every call returns a palu_status_t; nothing aborts, prints or throws.
  * Argument checks happen on the host before anything is queued. Conditions only
  * the GPU can see (a position outside the RoPE table, a sequence longer than
